@@ -1,0 +1,128 @@
+"""Seeded synthetic inputs for the prefill FP8 MQA indexer logits.
+
+This module holds no arithmetic of the method: it only draws inputs.  Both the CUDA
+path's tests/bench and the CPU oracle's tests take their inputs from here.
+
+Distributions (the same for every workload): Q and K are N(0,1) draws clipped to
++-448 and rounded to OCP E4M3 by torch's ``float8_e4m3fn`` conversion; w is
+N(0,1)/sqrt(H*D) in fp32; kv_scale is U[0.5, 2] in fp32.  One CPU ``torch.Generator``
+seeded with the workload's seed draws Q, K, w and kv_scale in that order.
+
+Window families.  The five benchmark workloads follow the kernel-time table of
+ROCm/aiter PR #7183 ("Kernel time on the GLM-5.3-Flash table shapes"): causal chunks
+whose query rows are the last M positions of an N-key context, and a multi-request
+chunk of four requests.  The test-only families ("cp", "misaligned", "empty",
+"past_end") are readings of the op-test window modes named in the same page's
+"Test plan"; the page does not define them, so each is spelled out below.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+
+import numpy as np
+import torch
+
+H_DEFAULT = 32
+D_DEFAULT = 128
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    M: int
+    N: int
+    windows: str  # window family, see ``windows()``
+    seed: int
+    H: int = H_DEFAULT
+    D: int = D_DEFAULT
+    requests: int = 1  # multi_req only
+
+
+# The five benchmark/parity workloads (seed = position in this list).
+WORKLOADS = {
+    "tiny_causal_64x256": Workload("tiny_causal_64x256", 64, 256, "causal", 0),
+    "causal_8192x8192": Workload("causal_8192x8192", 8192, 8192, "causal", 1),
+    "chunk_causal_4096x32768": Workload("chunk_causal_4096x32768", 4096, 32768, "causal", 2),
+    "long_causal_1024x131072": Workload("long_causal_1024x131072", 1024, 131072, "causal", 3),
+    "multi_req_4096x32768": Workload("multi_req_4096x32768", 4096, 32768, "multi_req", 4,
+                                     requests=4),
+}
+
+WINDOW_FAMILIES = ("causal", "cp", "misaligned", "empty", "past_end", "multi_req")
+
+
+def windows(family: str, M: int, N: int, requests: int = 4):
+    """Per-row [ks, ke) bounds (int32) for a window family.
+
+    causal     rows are the last M positions of an N-key context: ks=0, ke=N-M+m+1.
+    multi_req  ``requests`` requests, each owning a contiguous N/requests key segment
+               and M/requests query rows that are the last rows of that segment:
+               for request r, row i: ks = r*S, ke = r*S + (S - R) + i + 1 with
+               S = N/requests, R = M/requests.
+    cp         context-parallel split: the first half of the rows is causal at a
+               shifted, tile-unaligned offset, the second half is the tail chunk.
+    misaligned windows that start and end in the middle of key tiles.
+    empty      causal, but every third row is empty (ks == ke) and every seventh has
+               ks > ke.
+    past_end   ke beyond N for all rows, and some rows with ks >= N.
+    """
+    m = np.arange(M, dtype=np.int64)
+    if family == "causal":
+        ks = np.zeros(M, np.int64)
+        ke = (N - M) + m + 1
+    elif family == "multi_req":
+        if M % requests or N % requests:
+            raise ValueError("multi_req needs M and N divisible by the request count")
+        S, R = N // requests, M // requests
+        r, i = m // R, m % R
+        ks = r * S
+        ke = r * S + (S - R) + i + 1
+    elif family == "cp":
+        half = M // 2
+        off0 = max(0, (N - M) // 3 + 5)
+        ks = np.zeros(M, np.int64)
+        ke = np.where(m < half, off0 + m + 1, (N - (M - half)) + (m - half) + 1)
+    elif family == "misaligned":
+        span = max(1, N // 3)
+        ks = (37 * m + 5) % span
+        ke = ks + 1 + (101 * m + 11) % max(1, (2 * N) // 3)
+    elif family == "empty":
+        ks = np.zeros(M, np.int64)
+        ke = (N - M) + m + 1
+        ks = np.where(m % 3 == 1, ke, ks)
+        ks = np.where(m % 7 == 5, ke + 3, ks)
+    elif family == "past_end":
+        ks = (m * 13) % max(1, N)
+        ke = N + 17 + m
+        ks = np.where(m % 5 == 2, N + m % 3, ks)
+    else:
+        raise ValueError(f"unknown window family {family!r}")
+    return ks.astype(np.int32), ke.astype(np.int32)
+
+
+def draw(M: int, N: int, seed: int, H: int = H_DEFAULT, D: int = D_DEFAULT):
+    """Seeded Q, K, w, kv_scale as numpy arrays (q/k: uint8 E4M3 bytes)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    q = torch.randn((M, H, D), generator=g).clamp_(-448.0, 448.0).to(torch.float8_e4m3fn)
+    k = torch.randn((N, D), generator=g).clamp_(-448.0, 448.0).to(torch.float8_e4m3fn)
+    w = torch.randn((M, H), generator=g) / math.sqrt(H * D)
+    kv = torch.rand((N,), generator=g) * 1.5 + 0.5
+    return (q.view(torch.uint8).numpy(), k.view(torch.uint8).numpy(),
+            kv.to(torch.float32).numpy(), w.to(torch.float32).numpy())
+
+
+def make(wl: Workload, family: str | None = None):
+    """All host inputs for a workload: dict of numpy arrays plus sizes."""
+    q, k, kv, w = draw(wl.M, wl.N, wl.seed, wl.H, wl.D)
+    ks, ke = windows(family or wl.windows, wl.M, wl.N, wl.requests)
+    return {"q": q, "k": k, "kv_scale": kv, "w": w, "ks": ks, "ke": ke,
+            "M": wl.M, "N": wl.N, "H": wl.H, "D": wl.D}
+
+
+def valid_pairs(ks: np.ndarray, ke: np.ndarray, N: int) -> int:
+    """Number of in-window (m, n) pairs: sum over rows of |[ks,ke) clamped to [0,N)|."""
+    lo = np.clip(ks.astype(np.int64), 0, N)
+    hi = np.clip(ke.astype(np.int64), 0, N)
+    return int(np.maximum(hi - lo, 0).sum())
