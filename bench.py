@@ -1,0 +1,374 @@
+"""Benchmark of the prefill FP8 MQA indexer logits on one GB300 (or N replicas).
+
+A step is one call of the whole path (``fp8_mqa_logits``) on one batch of the
+causal 8192 x 8192 workload (H=32, D=128; the kernel-time table's first shape in
+ROCm/aiter PR #7183).  Inputs are resident in HBM before the timed region; L2 is
+flushed (a 256 MiB write) before every timed call, and each call is timed on the
+launching stream with CUDA events.  The metric is valid-window FP8 TFLOP/s:
+2*H*D*sum_m |window_m| per call over the call's device time.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                  [--impl reference] [--no-cpu-baseline]
+
+``--impl reference`` times the CPU oracle (test infrastructure) on the host cores on
+a bounded sample of the same workload and prints the same JSON line with
+"impl": "reference".
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "valid-window FP8 TFLOP/s and µs/call at 1 GB300; % of dense FP8 tensor peak"
+DEFAULT_WORKLOAD = "causal_8192x8192"
+FLUSH_BYTES = 256 << 20
+# the recipe's fallback peaks, used only when the measured file is absent
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+FP8_OVER_BF16 = 2.0  # nominal dense ratio 4.5 / 2.25 PFLOP/s
+REFERENCE_BUDGET_S = 90.0  # CPU seconds for a whole --impl reference run
+
+
+def valid_flops(inp) -> float:
+    return 2.0 * inp["H"] * inp["D"] * workloads.valid_pairs(inp["ks"], inp["ke"], inp["N"])
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            d = json.load(open(path))
+            return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                    "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained",
+                                                         d["bf16_tflops"])),
+                    "source": "measured"}
+        except Exception:
+            pass
+    return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS,
+            "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out = ""
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        rows = []
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append({"sm": float(f[1]), "max": float(f[2]), "power": float(f[3]),
+                             "hw": f[5], "hw_thermal": f[6], "sw_thermal": f[7],
+                             "sw_power": f[8]})
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        busy = [r for r in rows if r["power"] > 200.0] or rows
+        reasons = set()
+        for r in rows:
+            for key, name in (("hw", "hw_slowdown"), ("hw_thermal", "hw_thermal_slowdown"),
+                              ("sw_thermal", "sw_thermal_slowdown"),
+                              ("sw_power", "sw_power_cap")):
+                if r[key].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in busy),
+                "sm_max_mhz": max(r["max"] for r in rows), "reasons": sorted(reasons),
+                "samples": len(rows), "samples_under_load": len(busy)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    """Largest value over all ranks (the rank-aggregation the timing contract asks for)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    backend = dist.get_backend()
+    dev = "cuda" if backend == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def cpu_oracle_sample(inp, budget_rows: int, threads: int):
+    """Time the oracle on an evenly spaced sample of query rows; returns TFLOP/s etc."""
+    import oracle
+    M = inp["M"]
+    stride = max(1, M // budget_rows)
+    rows = np.arange(0, M, stride, dtype=np.int64)[:budget_rows]
+    pairs = workloads.valid_pairs(inp["ks"][rows], inp["ke"][rows], inp["N"])
+    flops = 2.0 * inp["H"] * inp["D"] * pairs
+    t0 = time.perf_counter()
+    oracle.fp8_mqa_logits(inp["q"], inp["k"], inp["kv_scale"], inp["w"], inp["ks"], inp["ke"],
+                          1, rows=rows, nthreads=threads)
+    dt = time.perf_counter() - t0
+    return {"tflops": flops / dt / 1e12, "seconds": dt, "rows": int(len(rows)),
+            "stride": int(stride), "flops": flops}
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    wl = workloads.WORKLOADS[args.workload]
+    inp = workloads.make(wl)
+    import oracle
+    oracle.build()
+    threads = oracle.default_threads()
+    # size each step so the whole run (warm-up + steps) takes about REFERENCE_BUDGET_S
+    probe = cpu_oracle_sample(inp, 64, threads)
+    per_row = probe["seconds"] / probe["rows"]
+    rows_per_step = int(REFERENCE_BUDGET_S / per_row / (args.steps + 0.25 * args.warmup))
+    rows_per_step = max(8, min(inp["M"], rows_per_step))
+    for _ in range(args.warmup):
+        cpu_oracle_sample(inp, max(8, rows_per_step // 4), threads)
+    samples = [cpu_oracle_sample(inp, rows_per_step, threads) for _ in range(args.steps)]
+    flops = sum(s["flops"] for s in samples)
+    secs = sum(s["seconds"] for s in samples)
+    value = flops / secs / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * secs / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "M": wl.M, "N": wl.N, "H": wl.H, "D": wl.D,
+                   "windows": "causal: ks=0, ke=N-M+m+1", "clean_logits": 1,
+                   "l2": "n/a (CPU)"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{samples[0]['rows']} query rows per step (every "
+                                   f"{samples[0]['stride']}th row) of {wl.name}, fp64 C "
+                                   f"oracle on {threads} host threads"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_gpu(args):
+    import torch
+
+    import fp8_mqa_logits_02_gb300 as fm
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    fm.lib()
+
+    wl = workloads.WORKLOADS[args.workload]
+    inp = workloads.make(wl)
+    M, N, H, D = inp["M"], inp["N"], inp["H"], inp["D"]
+    flops = valid_flops(inp)
+    q = torch.from_numpy(inp["q"]).to(dev).view(torch.float8_e4m3fn)
+    k = torch.from_numpy(inp["k"]).to(dev).view(torch.float8_e4m3fn)
+    kv = torch.from_numpy(inp["kv_scale"]).to(dev)
+    w = torch.from_numpy(inp["w"]).to(dev)
+    ks = torch.from_numpy(inp["ks"]).to(dev)
+    ke = torch.from_numpy(inp["ke"]).to(dev)
+    out = torch.empty((M, N), dtype=torch.float32, device=dev)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        fm.fp8_mqa_logits(q, k, kv, w, ks, ke, out=out, clean_logits=bool(args.clean),
+                          split_n=args.split_n, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    if fm.check_error(stream) != 0:
+        raise RuntimeError("device status after warm-up is not OK")
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(dev.index) as clocks:
+        for i in range(args.steps):
+            flush.zero_()
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+    if ws > 1:
+        torch.distributed.barrier()
+    status = fm.check_error(stream)
+    if status != 0:
+        raise RuntimeError(f"device status {fm.strerror(status)}")
+    ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = max_over_ranks(sum(ms), ws)
+    value = flops * args.steps * ws / (total_ms * 1e-3) / 1e12
+    per_launch_s = statistics.mean(ms) * 1e-3
+
+    # end to end through the host-buffer C entry point: pinned inputs copied in, the
+    # kernel, and the whole logits matrix copied back, every step
+    hq = torch.from_numpy(inp["q"]).pin_memory()
+    hk = torch.from_numpy(inp["k"]).pin_memory()
+    hkv = torch.from_numpy(inp["kv_scale"]).pin_memory()
+    hw = torch.from_numpy(inp["w"]).pin_memory()
+    hks = torch.from_numpy(inp["ks"]).pin_memory()
+    hke = torch.from_numpy(inp["ke"]).pin_memory()
+    hout = torch.empty((M, N), dtype=torch.float32).pin_memory()
+    wsp = torch.empty(fm.host_workspace_bytes(M, N), dtype=torch.uint8, device=dev)
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hkv, hw, hks, hke))
+    d2h = hout.numel() * 4
+
+    def e2e_step():
+        fm.fp8_mqa_logits_host(hq, hk, hkv, hw, hks, hke, hout, wsp,
+                               clean_logits=bool(args.clean), split_n=args.split_n,
+                               stream=stream)
+
+    e2e_steps = max(3, min(args.steps, 20))
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if ws > 1:
+        torch.distributed.barrier()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), ws)
+    e2e_value = flops * e2e_steps * ws / (e2e_ms * 1e-3) / 1e12
+    if fm.check_error(stream) != 0:
+        raise RuntimeError("device status after e2e is not OK")
+
+    peaks = load_peaks()
+    fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
+    achieved = flops / per_launch_s / 1e12
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tpath):
+        try:
+            tj = json.load(open(tpath))
+            if tj.get("workload") == wl.name and tj.get("kernel_rev") == KERNEL_REV:
+                traffic = tj.get("bytes_per_launch")
+        except Exception:
+            traffic = None
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total_ms / args.steps, "us_per_call": 1e3 * total_ms / args.steps,
+        "frac_of_fp8_peak": value / ws / fp8_peak,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp8e4m3*fp8e4m3->f32", "data": "synthetic",
+        "config": {"workload": wl.name, "M": M, "N": N, "H": H, "D": D,
+                   "windows": "causal: ks=0, ke=N-M+m+1" if wl.windows == "causal" else
+                   wl.windows, "clean_logits": int(args.clean), "split_n": args.split_n,
+                   "valid_flops_per_call": flops,
+                   "l2": f"flushed before every timed call ({FLUSH_BYTES >> 20} MiB write)",
+                   "timing": "CUDA events per call on the launching stream"},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": fp8_peak,
+                     "unit": "TFLOP/s", "frac": achieved / fp8_peak, "traffic": traffic,
+                     "peak_source": f"{peaks['source']} bf16 burst x {FP8_OVER_BF16:g} "
+                                    "(nominal fp8/bf16 ratio)",
+                     "kernel": "fp8_mqa_logits_kernel"},
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "entry": "fp8_mqa_logits_host (pinned host buffers)"},
+        "gpu_launches": args.steps,
+        "clocks": clocks.summary(),
+    }
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        threads = oracle.default_threads()
+        cb = cpu_oracle_sample(inp, args.reference_rows, threads)
+        line["cpu_baseline"] = {
+            "value": cb["tflops"], "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"{cb['rows']} query rows (every {cb['stride']}th) of {wl.name}, "
+                      f"fp64 C oracle, {cb['seconds']:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+# Revision tag of the kernel the committed ncu traffic figure was taken on.
+KERNEL_REV = "v1"
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--clean", type=int, default=1, choices=(0, 1))
+    ap.add_argument("--split-n", type=int, default=0)
+    ap.add_argument("--impl", default="native", choices=("native", "reference"))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--reference-rows", type=int, default=4096,
+                    help="query rows of the workload the CPU-baseline sample computes")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,193 @@
+"""Python binding of the GB300 prefill FP8 MQA indexer-logits library (``libfp8mqa.so``).
+
+Argument marshalling only: every step of the computation runs in the library's sm_103a
+kernel.  The binding refuses to work without the compiled library (it raises; there is
+no fallback).  The C entry points are declared in ``include/fp8_mqa_logits.h``.
+
+    out[m, n] = kv_scale[n] * sum_h relu(Q[m,h,:] . K[n,:]) * w[m,h]  for n in [ks[m], ke[m])
+    (ROCm/aiter PR #7183 "[HIP] [JIT] Add gfx950 prefill FP8 MQA logits", "Motivation")
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+HEADS = 32
+DIM = 128
+
+STATUS = {
+    0: "FP8MQA_OK",
+    -1: "FP8MQA_ERR_INVALID_ARG",
+    -2: "FP8MQA_ERR_UNSUPPORTED_SHAPE",
+    -3: "FP8MQA_ERR_MISALIGNED",
+    -4: "FP8MQA_ERR_ARCH",
+    -5: "FP8MQA_ERR_LAUNCH",
+    -6: "FP8MQA_ERR_TIMEOUT",
+    -7: "FP8MQA_ERR_CUDA",
+}
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libfp8mqa.so")
+_lock = threading.Lock()
+_lib = None
+
+# Every symbol the C header declares, with its ctypes signature.
+_P = ctypes.c_void_p
+_I64, _I32, _U64 = ctypes.c_int64, ctypes.c_int32, ctypes.c_uint64
+SIGNATURES = {
+    "fp8_mqa_logits": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I32, _I32, _I32,
+                                      _I32, _P]),
+    "fp8_mqa_logits_is_supported": (ctypes.c_int, [_I64, _I64, _I32, _I32]),
+    "fp8_mqa_logits_default_split": (ctypes.c_int, [_I64, _I64, _I32]),
+    "fp8_mqa_logits_check_error": (ctypes.c_int, [_P]),
+    "fp8_mqa_logits_host_workspace_bytes": (ctypes.c_uint64, [_I64, _I64, _I32, _I32]),
+    "fp8_mqa_logits_host": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I32, _I32,
+                                           _I32, _I32, _P, _U64, _P]),
+    "fp8_mqa_logits_strerror": (ctypes.c_char_p, [ctypes.c_int]),
+}
+
+
+class Fp8MqaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {strerror(status)} ({status})")
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile ``libfp8mqa.so`` in-tree with nvcc for sm_103a."""
+    import importlib
+    builder = importlib.import_module(__name__ + ".build")
+    return builder.build(force=force, verbose=verbose)
+
+
+def lib():
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"{LIB_PATH} is missing: build it with "
+                    "`python -m fp8_mqa_logits_02_gb300.build` (there is no CPU fallback)")
+            handle = ctypes.CDLL(LIB_PATH)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(handle, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = handle
+    return _lib
+
+
+def strerror(status: int) -> str:
+    try:
+        return lib().fp8_mqa_logits_strerror(int(status)).decode()
+    except Exception:  # library missing: fall back to the table above
+        return STATUS.get(int(status), f"unknown status {status}")
+
+
+def is_supported(M: int, N: int, H: int = HEADS, D: int = DIM) -> bool:
+    return bool(lib().fp8_mqa_logits_is_supported(M, N, H, D))
+
+
+def default_split(M: int, N: int, num_sms: int) -> int:
+    return int(lib().fp8_mqa_logits_default_split(M, N, num_sms))
+
+
+def _stream_ptr(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+def _check(t: torch.Tensor, name: str, dtypes, ndim: int, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name} must have dtype in {dtypes}, got {t.dtype}")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must be {ndim}-D, got shape {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+FP8 = (torch.float8_e4m3fn,)
+
+
+def fp8_mqa_logits(q: torch.Tensor, k: torch.Tensor, kv_scale: torch.Tensor, w: torch.Tensor,
+                   ks: torch.Tensor, ke: torch.Tensor, out: torch.Tensor | None = None,
+                   clean_logits: bool = True, split_n: int = 0, stream=None) -> torch.Tensor:
+    """Logits of every query row against its key window, on the GPU.
+
+    q: float8_e4m3fn [M, 32, 128]; k: float8_e4m3fn [N, 128]; kv_scale: float32 [N];
+    w: float32 [M, 32]; ks, ke: int32 [M] (row m attends keys ks[m] <= n < ke[m]).
+    out: optional float32 [M, N] to write into (needed to keep caller-managed values
+    with ``clean_logits=False``).  Returns ``out``.  Asynchronous on ``stream``
+    (default: the current stream).
+    """
+    _check(q, "q", FP8, 3)
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("q must be a CUDA tensor (the library has no CPU path)")
+    _check(k, "k", FP8, 2, dev)
+    _check(kv_scale, "kv_scale", (torch.float32,), 1, dev)
+    _check(w, "w", (torch.float32,), 2, dev)
+    _check(ks, "ks", (torch.int32,), 1, dev)
+    _check(ke, "ke", (torch.int32,), 1, dev)
+    M, H, D = q.shape
+    N = k.shape[0]
+    if k.shape[1] != D or tuple(w.shape) != (M, H) or kv_scale.shape[0] != N \
+            or ks.shape[0] != M or ke.shape[0] != M:
+        raise ValueError("inconsistent shapes")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=dev)
+    else:
+        _check(out, "out", (torch.float32,), 2, dev)
+        if tuple(out.shape) != (M, N):
+            raise ValueError(f"out must be [{M}, {N}]")
+    with torch.cuda.device(dev):
+        rc = lib().fp8_mqa_logits(q.data_ptr(), k.data_ptr(), kv_scale.data_ptr(), w.data_ptr(),
+                                  ks.data_ptr(), ke.data_ptr(), out.data_ptr(), M, N, H, D,
+                                  1 if clean_logits else 0, int(split_n), _stream_ptr(stream))
+    if rc != 0:
+        raise Fp8MqaError(rc, "fp8_mqa_logits")
+    return out
+
+
+def check_error(stream=None) -> int:
+    """Synchronize ``stream`` and return (and clear) the device status: 0 or a status code."""
+    return int(lib().fp8_mqa_logits_check_error(_stream_ptr(stream)))
+
+
+def host_workspace_bytes(M: int, N: int, H: int = HEADS, D: int = DIM) -> int:
+    return int(lib().fp8_mqa_logits_host_workspace_bytes(M, N, H, D))
+
+
+def fp8_mqa_logits_host(q, k, kv_scale, w, ks, ke, out, workspace: torch.Tensor,
+                        clean_logits: bool = True, split_n: int = 0, stream=None) -> None:
+    """Same operation on HOST tensors (pinned for asynchronous copies).
+
+    q/k: CPU uint8 or float8_e4m3fn; kv_scale, w: CPU float32; ks, ke: CPU int32;
+    out: CPU float32 [M, N], filled when ``stream`` is synchronized.  ``workspace`` is a
+    CUDA uint8 tensor of at least ``host_workspace_bytes(M, N)`` bytes.
+    """
+    for t, name in ((q, "q"), (k, "k"), (kv_scale, "kv_scale"), (w, "w"), (ks, "ks"),
+                    (ke, "ke"), (out, "out")):
+        if t.device.type != "cpu" or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CPU tensor")
+    M, H, D = q.shape
+    N = k.shape[0]
+    if workspace.device.type != "cuda" or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    with torch.cuda.device(workspace.device):
+        rc = lib().fp8_mqa_logits_host(
+            q.data_ptr(), k.data_ptr(), kv_scale.data_ptr(), w.data_ptr(), ks.data_ptr(),
+            ke.data_ptr(), out.data_ptr(), M, N, H, D, 1 if clean_logits else 0, int(split_n),
+            workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+            _stream_ptr(stream))
+    if rc != 0:
+        raise Fp8MqaError(rc, "fp8_mqa_logits_host")

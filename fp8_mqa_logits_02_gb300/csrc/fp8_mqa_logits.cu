@@ -1,0 +1,348 @@
+// Host side of the C ABI declared in include/fp8_mqa_logits.h: argument validation,
+// per-device state (scheduler slots, status word), TMA tensor maps, split choice and
+// the launch.  The device code is in logits_kernel.cuh.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <functional>
+#include <mutex>
+
+#include "../../include/fp8_mqa_logits.h"
+#include "logits_kernel.cuh"
+
+namespace fp8mqa {
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr uint32_t kSchedSlots = 64;        // concurrent launches per device before reuse
+constexpr uint64_t kTimeoutNs = 1000000000ull;  // bounded device waits give up after 1 s
+
+struct DeviceState {
+    std::once_flag once;
+    int init_status = FP8MQA_OK;
+    int sm_count = 0;
+    SchedSlot* sched = nullptr;  // kSchedSlots slots, zeroed
+    int32_t* status = nullptr;   // one status word
+    std::atomic<uint32_t> seq{0};
+};
+
+DeviceState g_dev[kMaxDevices];
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+void load_encode()
+{
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess) {
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// One-time per-device setup: architecture check, kernel attributes, library buffers.
+void init_device(int dev, DeviceState& st)
+{
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&st.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        st.init_status = FP8MQA_ERR_CUDA;
+        return;
+    }
+    if (major != 10 || minor != 3) {
+        st.init_status = FP8MQA_ERR_ARCH;
+        return;
+    }
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, fp8_mqa_logits_kernel) != cudaSuccess) {
+        st.init_status = FP8MQA_ERR_LAUNCH;
+        return;
+    }
+    // setmaxnreg redistributes exactly the launch allocation; any other register count
+    // would make the epilogue's request unsatisfiable, so refuse to launch.
+    if (uint32_t(fa.numRegs) != kLaunchRegs) {
+        st.init_status = FP8MQA_ERR_LAUNCH;
+        return;
+    }
+    if (cudaFuncSetAttribute(fp8_mqa_logits_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(kSmemBytes)) != cudaSuccess) {
+        st.init_status = FP8MQA_ERR_LAUNCH;
+        return;
+    }
+    void* buf = nullptr;
+    const size_t bytes = kSchedSlots * sizeof(SchedSlot) + 256;
+    if (cudaMalloc(&buf, bytes) != cudaSuccess) {
+        st.init_status = FP8MQA_ERR_CUDA;
+        return;
+    }
+    if (cudaMemset(buf, 0, bytes) != cudaSuccess) {
+        cudaFree(buf);
+        st.init_status = FP8MQA_ERR_CUDA;
+        return;
+    }
+    st.sched = static_cast<SchedSlot*>(buf);
+    st.status = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(buf) +
+                                           kSchedSlots * sizeof(SchedSlot));
+    std::call_once(g_encode_once, load_encode);
+    if (!g_encode) st.init_status = FP8MQA_ERR_CUDA;
+}
+
+DeviceState* device_state(int* err)
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        *err = FP8MQA_ERR_CUDA;
+        return nullptr;
+    }
+    DeviceState& st = g_dev[dev];
+    std::call_once(st.once, init_device, dev, std::ref(st));
+    if (st.init_status != FP8MQA_OK) {
+        *err = st.init_status;
+        return nullptr;
+    }
+    *err = FP8MQA_OK;
+    return &st;
+}
+
+bool encode(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t rank, const void* base,
+            const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box,
+            CUtensorMapSwizzle swizzle)
+{
+    const cuuint32_t elem_strides[2] = {1, 1};
+    return g_encode(map, dtype, rank, const_cast<void*>(base), dims, strides, box, elem_strides,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int check_args(const uint8_t* q, const uint8_t* k, const float* kv, const float* w,
+               const int32_t* ks, const int32_t* ke, const float* out, int64_t M, int64_t N,
+               int32_t H, int32_t D, int32_t clean, int32_t split_n)
+{
+    if (M < 0 || N < 0 || split_n < 0 || (clean != 0 && clean != 1))
+        return FP8MQA_ERR_INVALID_ARG;
+    if (!fp8_mqa_logits_is_supported(M, N, H, D)) return FP8MQA_ERR_UNSUPPORTED_SHAPE;
+    if (M == 0 || N == 0) return FP8MQA_OK;
+    if (!q || !k || !kv || !w || !ks || !ke || !out) return FP8MQA_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(kv, 16) || !aligned(w, 16) ||
+        !aligned(ks, 4) || !aligned(ke, 4) || !aligned(out, 4))
+        return FP8MQA_ERR_MISALIGNED;
+    return FP8MQA_OK;
+}
+
+int launch(const uint8_t* q, const uint8_t* k, const float* kv, const float* w,
+           const int32_t* ks, const int32_t* ke, float* out, int64_t M, int64_t N,
+           int32_t clean, int32_t split_n, cudaStream_t stream)
+{
+    int err = FP8MQA_OK;
+    DeviceState* st = device_state(&err);
+    if (!st) return err;
+
+    const int32_t num_tiles = int32_t((N + kTileKeys - 1) / kTileKeys);
+    int32_t split = split_n > 0 ? split_n : fp8_mqa_logits_default_split(M, N, st->sm_count);
+    if (split > num_tiles) split = num_tiles;
+    if (split < 1) split = 1;
+    const int32_t tpc = (num_tiles + split - 1) / split;
+    split = (num_tiles + tpc - 1) / tpc;  // drop chunks that would be empty
+    const int64_t num_blocks = (M + kRows - 1) / kRows;
+    const int64_t num_units = num_blocks * split;
+    if (num_units > INT32_MAX) return FP8MQA_ERR_UNSUPPORTED_SHAPE;
+
+    CUtensorMap tm_q, tm_k, tm_w, tm_kv;
+    {
+        const cuuint64_t dims[2] = {cuuint64_t(kDim), cuuint64_t(M) * kHeads};
+        const cuuint64_t strides[1] = {cuuint64_t(kDim)};
+        const cuuint32_t box[2] = {kDim, kUmmaN};
+        if (!encode(&tm_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, q, dims, strides, box,
+                    CU_TENSOR_MAP_SWIZZLE_128B))
+            return FP8MQA_ERR_LAUNCH;
+    }
+    {
+        const cuuint64_t dims[2] = {cuuint64_t(kDim), cuuint64_t(N)};
+        const cuuint64_t strides[1] = {cuuint64_t(kDim)};
+        const cuuint32_t box[2] = {kDim, kTileKeys};
+        if (!encode(&tm_k, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, k, dims, strides, box,
+                    CU_TENSOR_MAP_SWIZZLE_128B))
+            return FP8MQA_ERR_LAUNCH;
+    }
+    {
+        const cuuint64_t dims[2] = {cuuint64_t(kHeads), cuuint64_t(M)};
+        const cuuint64_t strides[1] = {cuuint64_t(kHeads) * 4};
+        const cuuint32_t box[2] = {kHeads, kRows};
+        if (!encode(&tm_w, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, w, dims, strides, box,
+                    CU_TENSOR_MAP_SWIZZLE_NONE))
+            return FP8MQA_ERR_LAUNCH;
+    }
+    {
+        const cuuint64_t dims[1] = {cuuint64_t(N)};
+        const cuuint64_t strides[1] = {0};
+        const cuuint32_t box[1] = {kTileKeys};
+        if (!encode(&tm_kv, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 1, kv, dims, strides, box,
+                    CU_TENSOR_MAP_SWIZZLE_NONE))
+            return FP8MQA_ERR_LAUNCH;
+    }
+
+    Params p;
+    p.ks = ks;
+    p.ke = ke;
+    p.out = out;
+    p.M = M;
+    p.N = N;
+    p.num_tiles = num_tiles;
+    p.tiles_per_chunk = tpc;
+    p.split = split;
+    p.num_blocks = int32_t(num_blocks);
+    p.num_units = int32_t(num_units);
+    p.clean = clean;
+    p.sched = st->sched + (st->seq.fetch_add(1, std::memory_order_relaxed) % kSchedSlots);
+    p.status = st->status;
+    p.timeout_ns = kTimeoutNs;
+
+    const int64_t grid = num_units < st->sm_count ? num_units : st->sm_count;
+    fp8_mqa_logits_kernel<<<unsigned(grid), kThreads, kSmemBytes, stream>>>(tm_q, tm_k, tm_w,
+                                                                           tm_kv, p);
+    if (cudaGetLastError() != cudaSuccess) return FP8MQA_ERR_LAUNCH;
+    return FP8MQA_OK;
+}
+
+uint64_t align256(uint64_t x) { return (x + 255) & ~uint64_t(255); }
+
+}  // namespace
+}  // namespace fp8mqa
+
+extern "C" {
+
+int fp8_mqa_logits_is_supported(int64_t M, int64_t N, int32_t H, int32_t D)
+{
+    if (H != fp8mqa::kHeads || D != fp8mqa::kDim) return 0;
+    if (M < 0 || N < 0) return 0;
+    if (M * int64_t(H) >= (int64_t(1) << 31)) return 0;
+    if (N >= (int64_t(1) << 31)) return 0;
+    return 1;
+}
+
+int fp8_mqa_logits_default_split(int64_t M, int64_t N, int32_t num_sms)
+{
+    // Enough units for the dynamic scheduler to balance (about 8 per SM when there are
+    // few row blocks), but chunks of at least 8 key tiles so Q reloads stay negligible.
+    if (M <= 0 || N <= 0) return 1;
+    if (num_sms < 1) num_sms = 1;
+    const int64_t tiles = (N + fp8mqa::kTileKeys - 1) / fp8mqa::kTileKeys;
+    const int64_t blocks = (M + fp8mqa::kRows - 1) / fp8mqa::kRows;
+    const int64_t target = int64_t(8) * num_sms;
+    int64_t s = (target + blocks - 1) / blocks;
+    const int64_t cap = tiles / 8 > 1 ? tiles / 8 : 1;
+    if (s > cap) s = cap;
+    if (s < 1) s = 1;
+    return int(s);
+}
+
+int fp8_mqa_logits(const uint8_t* q_fp8, const uint8_t* k_fp8, const float* kv_scale,
+                   const float* w, const int32_t* ks, const int32_t* ke, float* out, int64_t M,
+                   int64_t N, int32_t H, int32_t D, int32_t clean_logits, int32_t split_n,
+                   void* stream)
+{
+    const int rc =
+        fp8mqa::check_args(q_fp8, k_fp8, kv_scale, w, ks, ke, out, M, N, H, D, clean_logits,
+                           split_n);
+    if (rc != FP8MQA_OK || M == 0 || N == 0) return rc;
+    return fp8mqa::launch(q_fp8, k_fp8, kv_scale, w, ks, ke, out, M, N, clean_logits, split_n,
+                          static_cast<cudaStream_t>(stream));
+}
+
+int fp8_mqa_logits_check_error(void* stream)
+{
+    int err = FP8MQA_OK;
+    fp8mqa::DeviceState* st = fp8mqa::device_state(&err);
+    if (!st) return err;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return FP8MQA_ERR_CUDA;
+    int32_t word = 0;
+    if (cudaMemcpy(&word, st->status, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return FP8MQA_ERR_CUDA;
+    if (word != 0) {
+        const int32_t zero = 0;
+        if (cudaMemcpy(st->status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+            return FP8MQA_ERR_CUDA;
+        return FP8MQA_ERR_TIMEOUT;
+    }
+    return FP8MQA_OK;
+}
+
+uint64_t fp8_mqa_logits_host_workspace_bytes(int64_t M, int64_t N, int32_t H, int32_t D)
+{
+    if (!fp8_mqa_logits_is_supported(M, N, H, D)) return 0;
+    using fp8mqa::align256;
+    const uint64_t m = uint64_t(M), n = uint64_t(N);
+    return align256(m * H * D) + align256(n * D) + align256(n * 4) + align256(m * H * 4) +
+           align256(m * 4) * 2 + align256(m * n * 4);
+}
+
+int fp8_mqa_logits_host(const uint8_t* q_fp8, const uint8_t* k_fp8, const float* kv_scale,
+                        const float* w, const int32_t* ks, const int32_t* ke, float* out,
+                        int64_t M, int64_t N, int32_t H, int32_t D, int32_t clean_logits,
+                        int32_t split_n, void* workspace, uint64_t workspace_bytes,
+                        void* stream)
+{
+    int rc = fp8mqa::check_args(q_fp8, k_fp8, kv_scale, w, ks, ke, out, M, N, H, D,
+                                clean_logits, split_n);
+    if (rc != FP8MQA_OK || M == 0 || N == 0) return rc;
+    if (!workspace) return FP8MQA_ERR_INVALID_ARG;
+    if (!fp8mqa::aligned(workspace, 256)) return FP8MQA_ERR_MISALIGNED;
+    if (workspace_bytes < fp8_mqa_logits_host_workspace_bytes(M, N, H, D))
+        return FP8MQA_ERR_INVALID_ARG;
+    using fp8mqa::align256;
+    const uint64_t m = uint64_t(M), n = uint64_t(N);
+    uint8_t* base = static_cast<uint8_t*>(workspace);
+    uint8_t* dq = base;
+    uint8_t* dk = dq + align256(m * H * D);
+    float* dkv = reinterpret_cast<float*>(dk + align256(n * D));
+    float* dw = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(dkv) + align256(n * 4));
+    int32_t* dks = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(dw) + align256(m * H * 4));
+    int32_t* dke = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(dks) + align256(m * 4));
+    float* dout = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(dke) + align256(m * 4));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const cudaMemcpyKind h2d = cudaMemcpyHostToDevice;
+    if (cudaMemcpyAsync(dq, q_fp8, m * H * D, h2d, s) != cudaSuccess ||
+        cudaMemcpyAsync(dk, k_fp8, n * D, h2d, s) != cudaSuccess ||
+        cudaMemcpyAsync(dkv, kv_scale, n * 4, h2d, s) != cudaSuccess ||
+        cudaMemcpyAsync(dw, w, m * H * 4, h2d, s) != cudaSuccess ||
+        cudaMemcpyAsync(dks, ks, m * 4, h2d, s) != cudaSuccess ||
+        cudaMemcpyAsync(dke, ke, m * 4, h2d, s) != cudaSuccess)
+        return FP8MQA_ERR_CUDA;
+    if (!clean_logits && cudaMemcpyAsync(dout, out, m * n * 4, h2d, s) != cudaSuccess)
+        return FP8MQA_ERR_CUDA;
+    rc = fp8mqa::launch(dq, dk, dkv, dw, dks, dke, dout, M, N, clean_logits, split_n, s);
+    if (rc != FP8MQA_OK) return rc;
+    if (cudaMemcpyAsync(out, dout, m * n * 4, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return FP8MQA_ERR_CUDA;
+    return FP8MQA_OK;
+}
+
+const char* fp8_mqa_logits_strerror(int status)
+{
+    switch (status) {
+        case FP8MQA_OK: return "FP8MQA_OK";
+        case FP8MQA_ERR_INVALID_ARG: return "FP8MQA_ERR_INVALID_ARG: invalid argument";
+        case FP8MQA_ERR_UNSUPPORTED_SHAPE:
+            return "FP8MQA_ERR_UNSUPPORTED_SHAPE: needs H=32, D=128 and sizes within limits";
+        case FP8MQA_ERR_MISALIGNED: return "FP8MQA_ERR_MISALIGNED: pointer alignment";
+        case FP8MQA_ERR_ARCH: return "FP8MQA_ERR_ARCH: device is not compute capability 10.3";
+        case FP8MQA_ERR_LAUNCH: return "FP8MQA_ERR_LAUNCH: kernel configuration or launch failed";
+        case FP8MQA_ERR_TIMEOUT: return "FP8MQA_ERR_TIMEOUT: a bounded device wait gave up";
+        case FP8MQA_ERR_CUDA: return "FP8MQA_ERR_CUDA: CUDA runtime error";
+        default: return "FP8MQA: unknown status";
+    }
+}
+
+}  // extern "C"

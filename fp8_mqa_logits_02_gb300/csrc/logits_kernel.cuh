@@ -1,0 +1,622 @@
+// The prefill FP8 MQA indexer-logits kernel for GB300 (sm_103a).
+//
+//   out[m, n] = kv_scale[n] * sum_h relu(Q[m,h,:] . K[n,:]) * w[m,h],  n in [ks[m], ke[m])
+//
+// (ROCm/aiter PR #7183 "[HIP] [JIT] Add gfx950 prefill FP8 MQA logits", "Motivation".)
+//
+// Work unit = (row block of kRows = 8 query rows, key chunk).  A persistent grid of one
+// CTA per SM pulls units from a global counter, heaviest row blocks first (the page's
+// "reverse_rows", section "Design / Grid choice"); key chunks are the page's SplitN.
+//
+// Warp roles in a 384-thread CTA:
+//   warp 0      producer: claims units, computes each unit's key-tile range from the
+//               window union of its rows, and streams Q+w (once per unit) and K+kv_scale
+//               tiles (once per unit) into shared memory with TMA (page: "K is read once
+//               per 32 rows" and "kv_scale is staged next to it", section "Design").
+//   warp 1      TMEM owner and MMA issuer: per 128-key tile, 4 tcgen05.mma (K = 32 each)
+//               of A = K tile [128 keys x 128] by B = Q block [8 rows x 32 heads = 256 x
+//               128], accumulating S[key, (row, head)] in fp32 in one of two TMEM buffers.
+//   warps 2-3   -inf writers (clean_logits = 1): fill every out-of-window span outside the
+//               computed tile range, on their own light-first unit order so the writes
+//               overlap the compute-heavy units (page: "With clean_logits the kernel writes
+//               -inf itself").
+//   warps 4-11  epilogue: thread = one key (TMEM lane), so one tcgen05.ld gives it the 32
+//               heads of one query row; relu, times w, head sum in registers (no cross-lane
+//               reduction), times kv_scale once per (m, n), then a coalesced store.  Tiles
+//               fully inside every row's window store without compare/select; boundary
+//               tiles are masked (page: "clean stages" vs "masked boundary stages").
+//
+// Keys sit on the MMA M axis (TMEM lanes) and (row, head) on the N axis: this transposes
+// the page's layout (query heads on the matrix rows) so that the head reduction is a sum
+// inside one thread instead of a cross-lane permutation.
+//
+// Every mbarrier wait is bounded (globaltimer): on expiry the CTA raises a shared abort
+// flag and a global status bit, drains its in-flight TMA and MMA work, frees TMEM and
+// returns.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+
+#include "sm103_ptx.cuh"
+
+namespace fp8mqa {
+
+constexpr int kHeads = 32;
+constexpr int kDim = 128;
+constexpr int kRows = 8;                  // query rows per unit
+constexpr int kTileKeys = 128;            // keys per tile (MMA M)
+constexpr int kUmmaN = kRows * kHeads;    // 256 (MMA N)
+constexpr int kUmmaK = 32;                // FP8 K per tcgen05.mma
+constexpr int kStages = 6;                // K / kv_scale ring depth
+constexpr int kQSlots = 2;
+constexpr int kUnitSlots = 4;
+constexpr int kAccBufs = 2;
+constexpr uint32_t kTmemCols = kAccBufs * kUmmaN;  // 512
+constexpr int kThreads = 384;
+constexpr int kEpiWarp0 = 4;
+constexpr int kEpiWarps = 8;
+constexpr int kRowsPerEpiWarp = 4;
+constexpr int kFillWarp0 = 2;
+constexpr int kFillWarps = 2;
+
+constexpr uint32_t kQBytes = kRows * kHeads * kDim;   // 32768
+constexpr uint32_t kWBytes = kRows * kHeads * 4;      // 1024
+constexpr uint32_t kKBytes = kTileKeys * kDim;        // 16384
+constexpr uint32_t kKvBytes = kTileKeys * 4;          // 512
+
+// Shared-memory layout, offsets from a 1024-byte aligned base.
+constexpr uint32_t kOffQ = 0;
+constexpr uint32_t kOffK = kOffQ + kQSlots * kQBytes;
+constexpr uint32_t kOffW = kOffK + kStages * kKBytes;
+constexpr uint32_t kOffKv = kOffW + kQSlots * kWBytes;
+constexpr uint32_t kOffBar = kOffKv + kStages * kKvBytes;
+
+constexpr int kBarKFull = 0;
+constexpr int kBarKEmpty = kBarKFull + kStages;
+constexpr int kBarQFull = kBarKEmpty + kStages;
+constexpr int kBarQEmpty = kBarQFull + kQSlots;
+constexpr int kBarAccFull = kBarQEmpty + kQSlots;
+constexpr int kBarAccEmpty = kBarAccFull + kAccBufs;
+constexpr int kBarUnitFull = kBarAccEmpty + kAccBufs;
+constexpr int kBarUnitEmpty = kBarUnitFull + kUnitSlots;
+constexpr int kBarDrain = kBarUnitEmpty + kUnitSlots;
+constexpr int kNumBars = kBarDrain + 1;
+
+struct UnitInfo {
+    int32_t m0;      // first query row
+    int32_t t0, t1;  // key tiles [t0, t1) computed by MMA + epilogue
+    int32_t flags;   // kUnitTerminate
+};
+constexpr int32_t kUnitTerminate = 1;
+
+constexpr uint32_t kOffUnits = kOffBar + kNumBars * 8;
+constexpr uint32_t kOffMisc = kOffUnits + kUnitSlots * sizeof(UnitInfo);
+constexpr uint32_t kSmemUsed = kOffMisc + 16;
+constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // slack for aligning the base
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+
+// Per-role register budgets (setmaxnreg); the sum must equal the launch allocation
+// 384 threads x 168 registers.
+constexpr uint32_t kLaunchRegs = 168;
+constexpr uint32_t kCtlRegs = 56;
+constexpr uint32_t kEpiRegs = 224;
+static_assert(128 * kCtlRegs + 256 * kEpiRegs <= kThreads * kLaunchRegs, "register split");
+
+// Status word bits.
+constexpr int32_t kStatusTimeout = 1;
+
+// Scheduler slot in global memory: work counters that the last CTA resets.
+struct SchedSlot {
+    uint32_t next_unit;
+    uint32_t next_fill;
+    uint32_t done_ctas;
+    uint32_t pad;
+};
+
+struct Params {
+    const int32_t* ks;
+    const int32_t* ke;
+    float* out;
+    int64_t M;
+    int64_t N;
+    int32_t num_tiles;        // ceil(N / 128)
+    int32_t tiles_per_chunk;  // ceil(num_tiles / split)
+    int32_t split;            // key chunks per row block
+    int32_t num_blocks;       // ceil(M / 8)
+    int32_t num_units;        // num_blocks * split
+    int32_t clean;
+    SchedSlot* sched;
+    int32_t* status;
+    uint64_t timeout_ns;
+};
+
+// tcgen05 instruction descriptor: D f32, A = B = E4M3, both K-major, M = 128, N = 256.
+constexpr uint32_t kIdesc = (1u << 4)                          // D format: f32
+                            | (0u << 7) | (0u << 10)           // A, B format: E4M3
+                            | (uint32_t(kUmmaN >> 3) << 17)    // N / 8
+                            | (uint32_t(kTileKeys >> 4) << 24);  // M / 16
+
+// Shared-memory matrix descriptor for a K-major operand whose rows are exactly 128 bytes,
+// stored with the 128-byte swizzle (8-row atoms of 1024 bytes, as TMA writes them).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr)
+{
+    uint64_t d = 0;
+    d |= uint64_t((saddr >> 4) & 0x3FFF);  // start address
+    d |= uint64_t(1) << 16;                // leading byte offset (unused with this swizzle)
+    d |= uint64_t(1024 >> 4) << 32;        // stride byte offset: next 8-row atom
+    d |= uint64_t(1) << 46;                // descriptor version
+    d |= uint64_t(2) << 61;                // 128-byte swizzle
+    return d;
+}
+
+struct Ctl {
+    volatile int32_t* abort;
+    int32_t* status;
+    uint64_t timeout_ns;
+};
+
+// Bounded single-thread wait.  Returns false when the CTA is aborting.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Ctl& c)
+{
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = ptx::globaltimer_ns();
+    while (true) {
+        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if (*c.abort) return false;
+        if (ptx::globaltimer_ns() - t0 > c.timeout_ns) {
+            *c.abort = 1;
+            atomicOr(c.status, kStatusTimeout);
+            return false;
+        }
+    }
+}
+
+// Bounded wait for a whole warp: lane 0 waits, then every lane observes the completed
+// phase itself (immediate) so each lane has acquired the barrier's data.
+__device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity, const Ctl& c)
+{
+    const int lane = threadIdx.x & 31;
+    int ok = 1;
+    if (lane == 0) ok = wait_bar(bar, parity, c) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (ok) {
+        for (uint32_t i = 0; i < (1u << 20) && !ptx::mbar_try_wait(bar, parity); ++i) {
+        }
+    }
+    return ok != 0;
+}
+
+// Drain: wait for a phase without looking at the abort flag (still time-bounded).
+__device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity, uint64_t timeout_ns)
+{
+    const uint64_t t0 = ptx::globaltimer_ns();
+    while (!ptx::mbar_try_wait(bar, parity)) {
+        if (ptx::globaltimer_ns() - t0 > timeout_ns) break;
+    }
+}
+
+__device__ __forceinline__ int64_t clamp64(int64_t v, int64_t lo, int64_t hi)
+{
+    return v < lo ? lo : (v > hi ? hi : v);
+}
+
+// Unit geometry shared by the producer and the -inf writers: row block b, chunk c.
+// Key tiles [t0, t1) are those of chunk c that meet the union of the block's windows.
+struct Geometry {
+    int32_t m0, t0, t1, ct0, ct1;
+};
+
+__device__ __forceinline__ Geometry unit_geometry(const Params& p, int32_t b, int32_t c)
+{
+    const int lane = threadIdx.x & 31;
+    Geometry g;
+    g.m0 = b * kRows;
+    int64_t lo = INT64_MAX, hi = INT64_MIN;
+    if (lane < kRows && g.m0 + lane < p.M) {
+        const int64_t m = g.m0 + lane;
+        const int64_t s = clamp64(p.ks[m], 0, p.N);
+        const int64_t e = clamp64(p.ke[m], 0, p.N);
+        if (s < e) {
+            lo = s;
+            hi = e;
+        }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const int64_t olo = __shfl_xor_sync(0xffffffffu, lo, off);
+        const int64_t ohi = __shfl_xor_sync(0xffffffffu, hi, off);
+        lo = olo < lo ? olo : lo;
+        hi = ohi > hi ? ohi : hi;
+    }
+    g.ct0 = c * p.tiles_per_chunk;
+    g.ct1 = min(g.ct0 + p.tiles_per_chunk, p.num_tiles);
+    g.t0 = g.ct0;
+    g.t1 = g.ct0;
+    if (lo < hi && g.ct0 < g.ct1) {
+        const int32_t a = int32_t(lo / kTileKeys);
+        const int32_t e = int32_t((hi + kTileKeys - 1) / kTileKeys);
+        g.t0 = max(g.ct0, a);
+        g.t1 = min(g.ct1, e);
+        if (g.t1 < g.t0) g.t1 = g.t0;
+    }
+    return g;
+}
+
+// Warp-cooperative -inf fill of row[a, e) with streaming 16-byte stores.
+__device__ __forceinline__ void fill_neg_inf(float* row, int64_t a, int64_t e)
+{
+    if (a >= e) return;
+    const int lane = threadIdx.x & 31;
+    const float ninf = __int_as_float(0xff800000u);
+    const uintptr_t addr = reinterpret_cast<uintptr_t>(row + a);
+    int64_t head = int64_t(((16u - (addr & 15u)) & 15u) >> 2);
+    if (head > e - a) head = e - a;
+    if (lane < head) __stcs(row + a + lane, ninf);
+    a += head;
+    const int64_t nvec = (e - a) >> 2;
+    float4* v = reinterpret_cast<float4*>(row + a);
+    const float4 n4 = make_float4(ninf, ninf, ninf, ninf);
+    for (int64_t i = lane; i < nvec; i += 32) __stcs(v + i, n4);
+    a += nvec * 4;
+    if (lane < e - a) __stcs(row + a + lane, ninf);
+}
+
+__device__ __forceinline__ float relu_dot_row(const uint32_t* s, const float2* w2)
+{
+    // sum_h max(s_h, 0) * w_h with four independent fp32x2 accumulators
+    float2 a0 = make_float2(0.f, 0.f), a1 = a0, a2 = a0, a3 = a0;
+#pragma unroll
+    for (int h = 0; h < kHeads; h += 8) {
+        a0 = __ffma2_rn(make_float2(fmaxf(__uint_as_float(s[h + 0]), 0.f),
+                                    fmaxf(__uint_as_float(s[h + 1]), 0.f)),
+                        w2[(h >> 1) + 0], a0);
+        a1 = __ffma2_rn(make_float2(fmaxf(__uint_as_float(s[h + 2]), 0.f),
+                                    fmaxf(__uint_as_float(s[h + 3]), 0.f)),
+                        w2[(h >> 1) + 1], a1);
+        a2 = __ffma2_rn(make_float2(fmaxf(__uint_as_float(s[h + 4]), 0.f),
+                                    fmaxf(__uint_as_float(s[h + 5]), 0.f)),
+                        w2[(h >> 1) + 2], a2);
+        a3 = __ffma2_rn(make_float2(fmaxf(__uint_as_float(s[h + 6]), 0.f),
+                                    fmaxf(__uint_as_float(s[h + 7]), 0.f)),
+                        w2[(h >> 1) + 3], a3);
+    }
+    const float2 b0 = __fadd2_rn(a0, a1);
+    const float2 b1 = __fadd2_rn(a2, a3);
+    const float2 c0 = __fadd2_rn(b0, b1);
+    return c0.x + c0.y;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    fp8_mqa_logits_kernel(const __grid_constant__ CUtensorMap tm_q,
+                          const __grid_constant__ CUtensorMap tm_k,
+                          const __grid_constant__ CUtensorMap tm_w,
+                          const __grid_constant__ CUtensorMap tm_kv, const Params p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_base = ptx::smem_addr(smem_raw);
+    const uint32_t pad = ((raw_base + 1023u) & ~1023u) - raw_base;
+    uint8_t* smem = smem_raw + pad;
+    const uint32_t sbase = raw_base + pad;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    auto bar = [&](int i) -> uint32_t { return sbase + kOffBar + 8u * uint32_t(i); };
+    UnitInfo* units = reinterpret_cast<UnitInfo*>(smem + kOffUnits);
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + kOffMisc);
+    volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(smem + kOffMisc + 4);
+    const Ctl ctl{abort_flag, p.status, p.timeout_ns};
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            ptx::mbar_init(bar(kBarKFull + i), 1);
+            ptx::mbar_init(bar(kBarKEmpty + i), 1 + kEpiWarps);
+        }
+        for (int i = 0; i < kQSlots; ++i) {
+            ptx::mbar_init(bar(kBarQFull + i), 1);
+            ptx::mbar_init(bar(kBarQEmpty + i), 1 + kEpiWarps);
+        }
+        for (int i = 0; i < kAccBufs; ++i) {
+            ptx::mbar_init(bar(kBarAccFull + i), 1);
+            ptx::mbar_init(bar(kBarAccEmpty + i), kEpiWarps);
+        }
+        for (int i = 0; i < kUnitSlots; ++i) {
+            ptx::mbar_init(bar(kBarUnitFull + i), 1);
+            ptx::mbar_init(bar(kBarUnitEmpty + i), 1 + kEpiWarps);
+        }
+        ptx::mbar_init(bar(kBarDrain), 1);
+        *abort_flag = 0;
+        ptx::mbar_init_fence();
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tensormap(&tm_q);
+        ptx::prefetch_tensormap(&tm_k);
+        ptx::prefetch_tensormap(&tm_w);
+        ptx::prefetch_tensormap(&tm_kv);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(sbase + kOffMisc, kTmemCols);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp < kEpiWarp0) ptx::regs_dec<kCtlRegs>();
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        const uint64_t pol_k = ptx::policy_evict_last();
+        const uint64_t pol_q = ptx::policy_evict_first();
+        uint32_t ui = 0, g = 0, qi = 0;
+        while (true) {
+            uint32_t u = 0;
+            int stop = 0;
+            if (lane == 0) {
+                u = atomicAdd(&p.sched->next_unit, 1u);
+                stop = (u >= uint32_t(p.num_units) || *abort_flag) ? 1 : 0;
+            }
+            u = __shfl_sync(0xffffffffu, u, 0);
+            stop = __shfl_sync(0xffffffffu, stop, 0);
+            UnitInfo info{0, 0, 0, 0};
+            if (stop) {
+                info.flags = kUnitTerminate;
+            } else {
+                const int32_t b = p.num_blocks - 1 - int32_t(u / uint32_t(p.split));
+                const int32_t c = int32_t(u % uint32_t(p.split));
+                const Geometry geo = unit_geometry(p, b, c);
+                info.m0 = geo.m0;
+                info.t0 = geo.t0;
+                info.t1 = geo.t1;
+            }
+            int ok = 1;
+            if (lane == 0) {
+                const uint32_t slot = ui % kUnitSlots;
+                ok = wait_bar(bar(kBarUnitEmpty + slot), ((ui / kUnitSlots) & 1u) ^ 1u, ctl);
+                if (ok) {
+                    units[slot] = info;
+                    ptx::mbar_arrive(bar(kBarUnitFull + slot));
+                }
+                if (ok && !(info.flags & kUnitTerminate) && info.t1 > info.t0) {
+                    const uint32_t qs = qi % kQSlots;
+                    ok = wait_bar(bar(kBarQEmpty + qs), ((qi / kQSlots) & 1u) ^ 1u, ctl);
+                    if (ok) {
+                        const uint32_t fb = bar(kBarQFull + qs);
+                        ptx::mbar_arrive_expect_tx(fb, kQBytes + kWBytes);
+                        ptx::tma_load_2d_hint(sbase + kOffQ + qs * kQBytes, &tm_q, fb, 0,
+                                              info.m0 * kHeads, pol_q);
+                        ptx::tma_load_2d(sbase + kOffW + qs * kWBytes, &tm_w, fb, 0, info.m0);
+                        ++qi;
+                    }
+                    for (int32_t t = info.t0; ok && t < info.t1; ++t) {
+                        const uint32_t st = g % kStages;
+                        ok = wait_bar(bar(kBarKEmpty + st), ((g / kStages) & 1u) ^ 1u, ctl);
+                        if (!ok) break;
+                        const uint32_t fb = bar(kBarKFull + st);
+                        ptx::mbar_arrive_expect_tx(fb, kKBytes + kKvBytes);
+                        ptx::tma_load_2d_hint(sbase + kOffK + st * kKBytes, &tm_k, fb, 0,
+                                              t * kTileKeys, pol_k);
+                        ptx::tma_load_1d(sbase + kOffKv + st * kKvBytes, &tm_kv, fb,
+                                         t * kTileKeys);
+                        ++g;
+                    }
+                }
+            }
+            ++ui;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok || (info.flags & kUnitTerminate)) break;
+        }
+        if (lane == 0) {
+            // Wait for any TMA load still in flight before the CTA can exit: only the last
+            // kStages K loads and the last kQSlots Q loads can be outstanding.
+            for (uint32_t j = (g > kStages ? g - kStages : 0); j < g; ++j)
+                drain_bar(bar(kBarKFull + j % kStages), (j / kStages) & 1u, p.timeout_ns);
+            for (uint32_t j = (qi > kQSlots ? qi - kQSlots : 0); j < qi; ++j)
+                drain_bar(bar(kBarQFull + j % kQSlots), (j / kQSlots) & 1u, p.timeout_ns);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            uint32_t ui = 0, g = 0, qi = 0;
+            bool ok = true;
+            while (ok) {
+                const uint32_t slot = ui % kUnitSlots;
+                if (!wait_bar(bar(kBarUnitFull + slot), (ui / kUnitSlots) & 1u, ctl)) break;
+                const UnitInfo info = units[slot];
+                ptx::mbar_arrive(bar(kBarUnitEmpty + slot));
+                ++ui;
+                if (info.flags & kUnitTerminate) break;
+                if (info.t1 <= info.t0) continue;
+                const uint32_t qs = qi % kQSlots;
+                if (!wait_bar(bar(kBarQFull + qs), (qi / kQSlots) & 1u, ctl)) break;
+                ++qi;
+                const uint64_t bdesc = sw128_desc(sbase + kOffQ + qs * kQBytes);
+                for (int32_t t = info.t0; t < info.t1; ++t) {
+                    const uint32_t st = g % kStages;
+                    const uint32_t ab = g & 1u;
+                    if (!wait_bar(bar(kBarKFull + st), (g / kStages) & 1u, ctl)) {
+                        ok = false;
+                        break;
+                    }
+                    if (!wait_bar(bar(kBarAccEmpty + ab), ((g >> 1) & 1u) ^ 1u, ctl)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const uint64_t adesc = sw128_desc(sbase + kOffK + st * kKBytes);
+                    const uint32_t d = tmem_base + ab * kUmmaN;
+#pragma unroll
+                    for (int k = 0; k < kDim / kUmmaK; ++k) {
+                        // advance 32 bytes along K inside the swizzle atom
+                        ptx::mma_f8f6f4(d, adesc + 2ull * k, bdesc + 2ull * k, kIdesc,
+                                        k > 0 ? 1u : 0u);
+                    }
+                    ptx::mma_commit(bar(kBarKEmpty + st));
+                    ptx::mma_commit(bar(kBarAccFull + ab));
+                    ++g;
+                }
+                if (!ok) break;
+                ptx::mma_commit(bar(kBarQEmpty + qs));
+            }
+            // all MMAs issued by this thread complete before TMEM can be released
+            ptx::mma_commit(bar(kBarDrain));
+            drain_bar(bar(kBarDrain), 0, p.timeout_ns);
+        }
+        __syncwarp();
+    } else if (warp < kEpiWarp0) {
+        // ------------------------------------------------------------ -inf writers
+        if (p.clean) {
+            while (true) {
+                uint32_t u = 0;
+                int stop = 0;
+                if (lane == 0) {
+                    u = atomicAdd(&p.sched->next_fill, 1u);
+                    stop = (u >= uint32_t(p.num_units) || *abort_flag) ? 1 : 0;
+                }
+                u = __shfl_sync(0xffffffffu, u, 0);
+                if (__shfl_sync(0xffffffffu, stop, 0)) break;
+                // light-first order: the blocks with the most -inf first
+                const int32_t b = int32_t(u / uint32_t(p.split));
+                const int32_t c = int32_t(u % uint32_t(p.split));
+                const Geometry geo = unit_geometry(p, b, c);
+                const int64_t col_lo = int64_t(geo.ct0) * kTileKeys;
+                const int64_t col_hi = min(int64_t(geo.ct1) * kTileKeys, p.N);
+                const bool any = geo.t1 > geo.t0;
+                const int64_t left_end = any ? int64_t(geo.t0) * kTileKeys : col_hi;
+                const int64_t right_beg = any ? min(int64_t(geo.t1) * kTileKeys, p.N) : col_hi;
+                for (int r = 0; r < kRows; ++r) {
+                    const int64_t m = int64_t(geo.m0) + r;
+                    if (m >= p.M) break;
+                    float* row = p.out + m * p.N;
+                    fill_neg_inf(row, col_lo, left_end);
+                    fill_neg_inf(row, right_beg, col_hi);
+                }
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        ptx::regs_inc<kEpiRegs>();
+        const int sp = warp & 3;                          // TMEM sub-partition
+        const int half = (warp - kEpiWarp0) >> 2;        // which 4 of the 8 rows
+        const uint32_t lane_base = uint32_t(sp * 32) << 16;
+        const float ninf = __int_as_float(0xff800000u);
+        uint32_t ui = 0, g = 0, qi = 0;
+        float2 w2[kRowsPerEpiWarp][kHeads / 2];
+        bool ok = true;
+        while (ok) {
+            const uint32_t slot = ui % kUnitSlots;
+            if (!wait_bar_warp(bar(kBarUnitFull + slot), (ui / kUnitSlots) & 1u, ctl)) break;
+            const UnitInfo info = units[slot];
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(bar(kBarUnitEmpty + slot));
+            ++ui;
+            if (info.flags & kUnitTerminate) break;
+            if (info.t1 <= info.t0) continue;
+
+            const uint32_t qs = qi % kQSlots;
+            if (!wait_bar_warp(bar(kBarQFull + qs), (qi / kQSlots) & 1u, ctl)) break;
+            ++qi;
+            {
+                const float4* wsrc = reinterpret_cast<const float4*>(
+                    smem + kOffW + qs * kWBytes + half * kRowsPerEpiWarp * kHeads * 4);
+#pragma unroll
+                for (int r = 0; r < kRowsPerEpiWarp; ++r) {
+#pragma unroll
+                    for (int j = 0; j < kHeads / 4; ++j) {
+                        const float4 v = wsrc[r * (kHeads / 4) + j];
+                        w2[r][2 * j] = make_float2(v.x, v.y);
+                        w2[r][2 * j + 1] = make_float2(v.z, v.w);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(bar(kBarQEmpty + qs));
+
+            int64_t rlo[kRowsPerEpiWarp], rhi[kRowsPerEpiWarp];
+            bool rok[kRowsPerEpiWarp];
+#pragma unroll
+            for (int r = 0; r < kRowsPerEpiWarp; ++r) {
+                const int64_t m = int64_t(info.m0) + half * kRowsPerEpiWarp + r;
+                rok[r] = m < p.M;
+                rlo[r] = rok[r] ? clamp64(p.ks[m], 0, p.N) : 0;
+                rhi[r] = rok[r] ? clamp64(p.ke[m], 0, p.N) : 0;
+            }
+
+            for (int32_t t = info.t0; t < info.t1; ++t) {
+                const uint32_t st = g % kStages;
+                const uint32_t ab = g & 1u;
+                if (!wait_bar_warp(bar(kBarKFull + st), (g / kStages) & 1u, ctl)) {
+                    ok = false;
+                    break;
+                }
+                const float kv = reinterpret_cast<const float*>(
+                    smem + kOffKv + st * kKvBytes)[sp * 32 + lane];
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(bar(kBarKEmpty + st));
+                if (!wait_bar_warp(bar(kBarAccFull + ab), (g >> 1) & 1u, ctl)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+
+                const int64_t n0 = int64_t(t) * kTileKeys;
+                const int64_t n = n0 + sp * 32 + lane;
+                const uint32_t taddr =
+                    tmem_base + lane_base + ab * kUmmaN + uint32_t(half * kRowsPerEpiWarp * kHeads);
+                float v[kRowsPerEpiWarp];
+#pragma unroll
+                for (int r = 0; r < kRowsPerEpiWarp; ++r) {
+                    uint32_t s[32];
+                    ptx::tmem_ld_32x32b_x32(taddr + uint32_t(r * kHeads), s);
+                    ptx::tmem_wait_ld();
+                    if (r == kRowsPerEpiWarp - 1) {
+                        // all of this warp's accumulator reads are done: release the buffer
+                        ptx::tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) ptx::mbar_arrive(bar(kBarAccEmpty + ab));
+                    }
+                    v[r] = relu_dot_row(s, w2[r]) * kv;
+                }
+#pragma unroll
+                for (int r = 0; r < kRowsPerEpiWarp; ++r) {
+                    if (!rok[r]) continue;
+                    float* dst = p.out + (int64_t(info.m0) + half * kRowsPerEpiWarp + r) * p.N;
+                    const bool full = n0 >= rlo[r] && n0 + kTileKeys <= rhi[r];
+                    if (full) {
+                        __stcs(dst + n, v[r]);  // clean tile: no compare/select
+                    } else if (n < p.N) {
+                        const bool inside = n >= rlo[r] && n < rhi[r];
+                        if (inside)
+                            __stcs(dst + n, v[r]);
+                        else if (p.clean)
+                            __stcs(dst + n, ninf);
+                    }
+                }
+                ++g;
+            }
+        }
+    }
+
+    // ---------------------------------------------------------------- teardown
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem_base, kTmemCols);
+    }
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const uint32_t prev = atomicAdd(&p.sched->done_ctas, 1u);
+        if (prev == gridDim.x - 1) {
+            // last CTA out: every producer and writer has stopped claiming work
+            p.sched->next_unit = 0;
+            p.sched->next_fill = 0;
+            p.sched->done_ctas = 0;
+            __threadfence();
+        }
+    }
+}
+
+}  // namespace fp8mqa

@@ -1,0 +1,144 @@
+/*
+ * fp8_mqa_logits.h -- C ABI of the GB300 (sm_103a) prefill FP8 MQA indexer-logits library.
+ *
+ * The operation (ROCm/aiter PR #7183 "[HIP] [JIT] Add gfx950 prefill FP8 MQA logits",
+ * section "Motivation", the displayed formula):
+ *
+ *     out[m, n] = kv_scale[n] * sum_{h < H} relu( Q[m,h,:] . K[n,:] ) * w[m,h]
+ *                 for n in [ks[m], ke[m]),   -inf elsewhere (clean_logits = 1).
+ *
+ * Operator contract (same page, "PR-specific question" and "Motivation"): H = 32 heads,
+ * D = 128 head dimension, FP8 Q/K, float32 kv_scale / w / out, int32 row bounds, all
+ * contiguous row-major.  FP8 here means OCP E4M3 ("e4m3fn", largest finite value 448).
+ *
+ * Conventions shared by every entry point below:
+ *   - All tensor pointers are DEVICE pointers (cudaMalloc / torch CUDA memory) owned by
+ *     the caller, unless an entry point says otherwise.  The library never frees them.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Compute entry
+ *     points are asynchronous and stream-ordered: they return after enqueueing work.
+ *   - Return value: FP8MQA_OK (0) or a negative fp8mqa_status.  Argument errors are
+ *     detected on the host BEFORE anything is enqueued; the library never aborts or
+ *     exits the process and throws no exceptions.
+ *   - The library keeps one small device buffer per device (a scheduler slot ring and a
+ *     status word, under 1 KB), allocated on the first compute call on that device and
+ *     kept until process exit.  That first call therefore must not be made while the
+ *     stream is being captured into a CUDA graph.
+ */
+#ifndef FP8_MQA_LOGITS_H
+#define FP8_MQA_LOGITS_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define FP8MQA_API __attribute__((visibility("default")))
+#else
+#define FP8MQA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. */
+enum fp8mqa_status {
+    FP8MQA_OK = 0,
+    FP8MQA_ERR_INVALID_ARG = -1,       /* null pointer, negative size, bad flag, bad split_n */
+    FP8MQA_ERR_UNSUPPORTED_SHAPE = -2, /* H != 32, D != 128, or a size beyond the limits   */
+    FP8MQA_ERR_MISALIGNED = -3,        /* q/k/w/kv_scale not 16-byte aligned, out/ks/ke not 4 */
+    FP8MQA_ERR_ARCH = -4,              /* current device is not compute capability 10.3     */
+    FP8MQA_ERR_LAUNCH = -5,            /* the kernel could not be configured or launched    */
+    FP8MQA_ERR_TIMEOUT = -6,           /* a bounded on-device wait gave up (see check_error) */
+    FP8MQA_ERR_CUDA = -7               /* a CUDA runtime call failed                        */
+};
+
+/*
+ * fp8_mqa_logits -- the logits of every query row against its key window.
+ *
+ *   q_fp8     [M, H, D] E4M3 bytes, row-major (query row m, head h, dim d at
+ *             (m*H + h)*D + d).  16-byte aligned.
+ *   k_fp8     [N, D] E4M3 bytes, row-major.  16-byte aligned.
+ *   kv_scale  [N] float32, per-key scale, applied after the head sum.  16-byte aligned.
+ *   w         [M, H] float32, per-(row, head) weight, applied after relu.  16-byte aligned.
+ *   ks, ke    [M] int32: row m attends keys n with ks[m] <= n < ke[m].  Bounds are
+ *             clamped to [0, N); ks[m] >= ke[m] is an empty row.  4-byte aligned.
+ *   out       [M, N] float32, row-major, 4-byte aligned.  In-window entries are always
+ *             written.  clean_logits = 1: every out-of-window entry is written with -inf
+ *             (IEEE 0xff800000), so the whole matrix is defined.  clean_logits = 0:
+ *             out-of-window entries are not written at all (they keep whatever the
+ *             caller put there; "caller-managed output masks", page section
+ *             "PR Self-Review / Behavior and intent").
+ *   M, N      query rows and keys (>= 0).  M = 0 or N = 0 enqueues nothing and returns OK.
+ *             Limits: M*H < 2^31, N < 2^31.
+ *   H, D      must be 32 and 128 (FP8MQA_ERR_UNSUPPORTED_SHAPE otherwise).
+ *   split_n   0 = automatic; > 0 = split each row block's key range into that many
+ *             chunks scheduled independently (the page's "SplitN", section "Design /
+ *             Grid choice" and "Known limitations").  Values above ceil(N/128) are
+ *             clamped.  The result is bit-identical for every split_n.
+ *   stream    cudaStream_t to enqueue on.
+ *
+ * Numerics: the dot products are exact (FP8 products accumulate in fp32 on the tensor
+ * cores); relu, the w-weighted head sum and the kv_scale multiply are fp32.
+ * Asynchronous device-side failures (a bounded wait that gave up) are reported by
+ * fp8_mqa_logits_check_error.
+ */
+FP8MQA_API int fp8_mqa_logits(const uint8_t* q_fp8, const uint8_t* k_fp8, const float* kv_scale,
+                   const float* w, const int32_t* ks, const int32_t* ke, float* out,
+                   int64_t M, int64_t N, int32_t H, int32_t D, int32_t clean_logits,
+                   int32_t split_n, void* stream);
+
+/*
+ * fp8_mqa_logits_is_supported -- 1 if (M, N, H, D) is inside this library's contract
+ * (H = 32, D = 128, M >= 0, N >= 0, M*H < 2^31, N < 2^31), else 0.  Pure host
+ * arithmetic: it touches no device and may be called without a GPU (the page's
+ * is_supported(), section "Motivation").
+ */
+FP8MQA_API int fp8_mqa_logits_is_supported(int64_t M, int64_t N, int32_t H, int32_t D);
+
+/*
+ * fp8_mqa_logits_default_split -- the split_n that split_n = 0 selects for an
+ * (M, N) problem on a GPU with `num_sms` multiprocessors.  Host arithmetic only.
+ */
+FP8MQA_API int fp8_mqa_logits_default_split(int64_t M, int64_t N, int32_t num_sms);
+
+/*
+ * fp8_mqa_logits_check_error -- synchronizes `stream`, then reads and clears the
+ * current device's status word.  Returns FP8MQA_ERR_TIMEOUT if any launch since the
+ * last check had a bounded on-device wait give up (its output is then incomplete),
+ * FP8MQA_ERR_CUDA if the synchronization itself failed, else FP8MQA_OK.
+ */
+FP8MQA_API int fp8_mqa_logits_check_error(void* stream);
+
+/*
+ * fp8_mqa_logits_host_workspace_bytes -- size of the device workspace that
+ * fp8_mqa_logits_host needs for an (M, N) problem (H = 32, D = 128), or 0 for a
+ * shape outside the contract.
+ */
+FP8MQA_API uint64_t fp8_mqa_logits_host_workspace_bytes(int64_t M, int64_t N, int32_t H, int32_t D);
+
+/*
+ * fp8_mqa_logits_host -- the same operation on HOST buffers.  Enqueues on `stream`:
+ * host->device copies of q, k, kv_scale, w, ks, ke into `workspace`, the kernel, and a
+ * device->host copy of all of out.  Host buffers should be pinned (cudaHostAlloc) for
+ * the copies to be asynchronous; pageable memory works but the copies then block.
+ * The call returns after enqueueing; synchronize `stream` before reading `out`.
+ * With clean_logits = 0, the device copy of out is first filled from the host `out`, so
+ * untouched entries come back unchanged.
+ *   workspace        device pointer, 256-byte aligned, at least
+ *                    fp8_mqa_logits_host_workspace_bytes(M, N, H, D) bytes, caller-owned.
+ *   workspace_bytes  its size.
+ * Other arguments as for fp8_mqa_logits.
+ */
+FP8MQA_API int fp8_mqa_logits_host(const uint8_t* q_fp8, const uint8_t* k_fp8, const float* kv_scale,
+                        const float* w, const int32_t* ks, const int32_t* ke, float* out,
+                        int64_t M, int64_t N, int32_t H, int32_t D, int32_t clean_logits,
+                        int32_t split_n, void* workspace, uint64_t workspace_bytes,
+                        void* stream);
+
+/* fp8_mqa_logits_strerror -- a static, human-readable name for a status code. */
+FP8MQA_API const char* fp8_mqa_logits_strerror(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8_MQA_LOGITS_H */

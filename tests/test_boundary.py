@@ -1,0 +1,120 @@
+"""The C-ABI boundary without a GPU: the library builds, loads, exports every symbol the
+header declares, and rejects bad arguments on the host before touching a device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import fp8_mqa_logits_02_gb300 as fm
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fp8_mqa_logits.h")
+
+OK, INVALID, UNSUPPORTED, MISALIGNED = 0, -1, -2, -3
+
+
+@pytest.fixture(scope="module")
+def lib():
+    fm.build()
+    return fm.lib()
+
+
+def header_functions():
+    text = open(HEADER).read()
+    return re.findall(r"FP8MQA_API\s+[\w\s\*]+?\b(fp8_mqa_logits\w*)\s*\(", text)
+
+
+def test_header_declares_expected_entry_points():
+    names = header_functions()
+    assert "fp8_mqa_logits" in names
+    assert len(names) == len(set(names)) == len(fm.SIGNATURES)
+    assert set(names) == set(fm.SIGNATURES)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    handle = ctypes.CDLL(fm.LIB_PATH)
+    for name in header_functions():
+        assert hasattr(handle, name), name
+
+
+def test_status_codes_match_header(lib):
+    text = open(HEADER).read()
+    codes = dict((int(v), k) for k, v in re.findall(r"(FP8MQA_\w+)\s*=\s*(-?\d+)", text))
+    assert codes == fm.STATUS
+    for code, name in codes.items():
+        assert lib.fp8_mqa_logits_strerror(code).decode().startswith(name)
+
+
+def test_is_supported_truth_table(lib):
+    assert fm.is_supported(8192, 8192)
+    assert fm.is_supported(0, 0)
+    assert fm.is_supported(1, 1)
+    assert not fm.is_supported(16, 16, H=64)
+    assert not fm.is_supported(16, 16, D=64)
+    assert not fm.is_supported(-1, 16)
+    assert not fm.is_supported(16, -1)
+    assert not fm.is_supported(2 ** 26, 16)       # M*H = 2^31
+    assert fm.is_supported(2 ** 26 - 1, 16)
+    assert not fm.is_supported(16, 2 ** 31)
+
+
+def test_default_split(lib):
+    # about 8 units per SM when row blocks are few, chunks of at least 8 key tiles
+    assert fm.default_split(8192, 8192, 152) == 2
+    assert fm.default_split(4096, 32768, 152) == 3
+    assert fm.default_split(1024, 131072, 152) == 10
+    assert fm.default_split(64, 256, 152) == 1
+    assert fm.default_split(1, 1, 152) == 1
+    for M in (1, 7, 100, 5000):
+        for N in (1, 129, 4000, 100000):
+            s = fm.default_split(M, N, 152)
+            assert 1 <= s <= max(1, -(-N // 128))
+
+
+def _call(lib, M=16, N=16, H=32, D=128, clean=1, split=0, ptrs=None):
+    p = ptrs or [0x1000] * 7
+    return lib.fp8_mqa_logits(*p, M, N, H, D, clean, split, None)
+
+
+def test_rejects_before_any_device_work(lib):
+    # fake but aligned pointers: validation must fail before they could be dereferenced
+    assert _call(lib, H=16) == UNSUPPORTED
+    assert _call(lib, D=64) == UNSUPPORTED
+    assert _call(lib, M=-1) == INVALID
+    assert _call(lib, N=-5) == INVALID
+    assert _call(lib, split=-1) == INVALID
+    assert _call(lib, clean=2) == INVALID
+    for i in range(7):
+        ptrs = [0x1000] * 7
+        ptrs[i] = None
+        assert _call(lib, ptrs=ptrs) == INVALID, i
+    for i, align in enumerate([16, 16, 16, 16, 4, 4, 4]):
+        ptrs = [0x1000] * 7
+        ptrs[i] = 0x1000 + (8 if align == 16 else 2)
+        assert _call(lib, ptrs=ptrs) == MISALIGNED, i
+    # empty problems are a no-op that never touches the device, even with null pointers
+    assert _call(lib, M=0, ptrs=[None] * 7) == OK
+    assert _call(lib, N=0, ptrs=[None] * 7) == OK
+
+
+def test_host_entry_rejects_bad_workspace(lib):
+    need = lib.fp8_mqa_logits_host_workspace_bytes(16, 16, 32, 128)
+    assert need > 16 * 16 * 4
+    assert lib.fp8_mqa_logits_host_workspace_bytes(16, 16, 16, 128) == 0
+    p = [0x1000] * 7
+    assert lib.fp8_mqa_logits_host(*p, 16, 16, 32, 128, 1, 0, None, need, None) == INVALID
+    assert lib.fp8_mqa_logits_host(*p, 16, 16, 32, 128, 1, 0, 0x1010, need, None) == MISALIGNED
+    assert lib.fp8_mqa_logits_host(*p, 16, 16, 32, 128, 1, 0, 0x1000, need - 1, None) == INVALID
+
+
+def test_binding_rejects_cpu_tensors(lib):
+    import torch
+    q = torch.zeros((4, 32, 128), dtype=torch.float8_e4m3fn)
+    k = torch.zeros((8, 128), dtype=torch.float8_e4m3fn)
+    with pytest.raises(ValueError, match="CUDA"):
+        fm.fp8_mqa_logits(q, k, torch.ones(8), torch.ones(4, 32),
+                          torch.zeros(4, dtype=torch.int32), torch.ones(4, dtype=torch.int32))
+    with pytest.raises(TypeError):
+        fm.fp8_mqa_logits(q.view(torch.uint8), k, torch.ones(8), torch.ones(4, 32),
+                          torch.zeros(4, dtype=torch.int32), torch.ones(4, dtype=torch.int32))

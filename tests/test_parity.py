@@ -1,0 +1,200 @@
+"""GPU parity: the sm_103a CUDA path, called through the C ABI, against the fp64 CPU oracle.
+
+Bar: the -inf mask bit-exact (IEEE 0xff800000 outside [ks, ke) with clean_logits=1,
+untouched poison with clean_logits=0) and every in-window value within
+1e-3 + 1e-3*|oracle| of the fp64 oracle, on the same seeded inputs.
+"""
+import numpy as np
+import pytest
+import torch
+
+import fp8_mqa_logits_02_gb300 as fm
+import workloads
+from gpu_helpers import (assert_parity, poisoned, run_gpu, run_oracle, to_device, window_mask)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    fm.build()
+    fm.lib()
+
+
+def _inputs(M, N, family, seed, requests=4):
+    q, k, kv, w = workloads.draw(M, N, seed)
+    ks, ke = workloads.windows(family, M, N, requests)
+    return {"q": q, "k": k, "kv_scale": kv, "w": w, "ks": ks, "ke": ke, "M": M, "N": N,
+            "H": 32, "D": 128}
+
+
+# ------------------------------------------------------------------ the tiny workload, full
+@pytest.mark.parametrize("clean", [True, False])
+@pytest.mark.parametrize("split_n", [0, 1, 2])
+def test_tiny_causal_full(clean, split_n):
+    inp = workloads.make(workloads.WORKLOADS["tiny_causal_64x256"])
+    gpu = run_gpu(inp, clean=clean, split_n=split_n)
+    ref = run_oracle(inp, clean=clean)
+    assert_parity(gpu, ref, window_mask(inp["ks"], inp["ke"], inp["N"]), clean,
+                  what=f"tiny clean={clean} split={split_n}")
+
+
+# ------------------------------------------------------------------ window families
+@pytest.mark.parametrize("family", workloads.WINDOW_FAMILIES)
+@pytest.mark.parametrize("clean", [True, False])
+def test_window_families(family, clean):
+    M, N = 96, 1040  # several row blocks and key tiles, ragged last tile
+    inp = _inputs(M, N, family, seed=17)
+    ref = run_oracle(inp, clean=clean)
+    inside = window_mask(inp["ks"], inp["ke"], N)
+    for split_n in (0, 1, 3, 20):
+        gpu = run_gpu(inp, clean=clean, split_n=split_n)
+        assert_parity(gpu, ref, inside, clean, what=f"{family} clean={clean} split={split_n}")
+
+
+# ------------------------------------------------------------------ ragged shapes
+@pytest.mark.parametrize("M", [1, 3, 8, 9, 127, 129])
+@pytest.mark.parametrize("N", [1, 127, 128, 129, 1000])
+def test_ragged_shapes(M, N):
+    for family in ("causal", "misaligned"):
+        inp = _inputs(M, N, family, seed=M * 1000 + N)
+        ref = run_oracle(inp, clean=True)
+        gpu = run_gpu(inp, clean=True)
+        assert_parity(gpu, ref, window_mask(inp["ks"], inp["ke"], N), True,
+                      what=f"M={M} N={N} {family}")
+
+
+def test_all_rows_empty_and_out_of_range():
+    M, N = 40, 700
+    inp = _inputs(M, N, "causal", seed=5)
+    inp["ks"] = np.array([(7 * m) % N + 3 for m in range(M)], np.int32)
+    inp["ke"] = inp["ks"] - (np.arange(M, dtype=np.int32) % 3)       # ks >= ke: empty
+    inp["ks"][::5] = N + 10                                            # starts past the end
+    inp["ke"][::5] = N + 50
+    inp["ks"][1::7] = -100                                             # negative, still empty
+    inp["ke"][1::7] = -3
+    gpu = run_gpu(inp, clean=True)
+    assert np.all(gpu.view(np.uint32) == 0xFF800000)
+    out0 = run_gpu(inp, clean=False)
+    assert np.all(out0.view(np.uint32) == 0x7FC0DEAD)
+
+
+# ------------------------------------------------------------------ invariants on the GPU
+def test_split_n_bit_identical_and_clean_consistent():
+    inp = _inputs(200, 3000, "misaligned", seed=9)
+    dev = to_device(inp)
+    base = run_gpu(inp, clean=True, split_n=1, dev=dev)
+    for split_n in (0, 2, 3, 7, 20, 24, 1000):
+        other = run_gpu(inp, clean=True, split_n=split_n, dev=dev)
+        assert np.array_equal(base.view(np.uint32), other.view(np.uint32)), split_n
+    unclean = run_gpu(inp, clean=False, split_n=5, dev=dev)
+    inside = window_mask(inp["ks"], inp["ke"], inp["N"])
+    assert np.array_equal(base.view(np.uint32)[inside], unclean.view(np.uint32)[inside])
+
+
+def test_wide_dynamic_range_codes():
+    # Q, K drawn uniformly over every finite E4M3 code (subnormals to +-448).  The dots
+    # then reach ~1e7 and fp32 accumulation on the tensor cores is the precision the
+    # page specifies, so the bound adds 2^-19 x sum_h relu(S)|w| kv (oracle with |w|).
+    rng = np.random.default_rng(3)
+    M, N = 64, 512
+    inp = _inputs(M, N, "misaligned", seed=3)
+    for name, shape in (("q", (M, 32, 128)), ("k", (N, 128))):
+        c = rng.integers(0, 256, size=shape, dtype=np.uint8)
+        inp[name] = np.where((c & 0x7F) == 0x7F, c & 0xF8, c).astype(np.uint8)
+    ref = run_oracle(inp, clean=True)
+    absw = dict(inp, w=np.abs(inp["w"]))
+    mag = np.abs(run_oracle(absw, clean=True))
+    mag[~np.isfinite(mag)] = 0
+    gpu = run_gpu(inp, clean=True)
+    assert_parity(gpu, ref, window_mask(inp["ks"], inp["ke"], N), True,
+                  extra_tol=mag * 2.0 ** -19, what="wide range")
+
+
+def test_many_calls_reuse_scheduler_slots():
+    # more calls than the library's per-device scheduler slots, back to back on one stream
+    inp = _inputs(24, 600, "misaligned", seed=11)
+    dev = to_device(inp)
+    ref = run_oracle(inp, clean=True)
+    inside = window_mask(inp["ks"], inp["ke"], inp["N"])
+    outs = [poisoned(24, 600) for _ in range(70)]
+    for i, o in enumerate(outs):
+        fm.fp8_mqa_logits(dev["q"], dev["k"], dev["kv_scale"], dev["w"], dev["ks"], dev["ke"],
+                          out=o, clean_logits=True, split_n=i % 4)
+    assert fm.check_error() == 0
+    for o in outs:
+        assert_parity(o.cpu().numpy(), ref, inside, True, what="repeat")
+
+
+def test_two_streams_concurrently():
+    inp = _inputs(300, 2500, "causal", seed=12)
+    dev = to_device(inp)
+    ref = run_oracle(inp, clean=True)
+    inside = window_mask(inp["ks"], inp["ke"], inp["N"])
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    o1, o2 = poisoned(300, 2500), poisoned(300, 2500)
+    torch.cuda.synchronize()
+    fm.fp8_mqa_logits(dev["q"], dev["k"], dev["kv_scale"], dev["w"], dev["ks"], dev["ke"],
+                      out=o1, stream=s1)
+    fm.fp8_mqa_logits(dev["q"], dev["k"], dev["kv_scale"], dev["w"], dev["ks"], dev["ke"],
+                      out=o2, stream=s2, split_n=3)
+    torch.cuda.synchronize()
+    assert fm.check_error() == 0
+    assert_parity(o1.cpu().numpy(), ref, inside, True, what="stream 1")
+    assert_parity(o2.cpu().numpy(), ref, inside, True, what="stream 2")
+
+
+def test_host_buffer_entry_point():
+    inp = _inputs(50, 900, "multi_req", seed=13, requests=2)
+    ref = run_oracle(inp, clean=True)
+    cpu = {k: torch.from_numpy(inp[k]).pin_memory()
+           for k in ("q", "k", "kv_scale", "w", "ks", "ke")}
+    out = torch.empty((50, 900), dtype=torch.float32).pin_memory()
+    ws = torch.empty(fm.host_workspace_bytes(50, 900), dtype=torch.uint8, device="cuda")
+    fm.fp8_mqa_logits_host(cpu["q"], cpu["k"], cpu["kv_scale"], cpu["w"], cpu["ks"], cpu["ke"],
+                           out, ws)
+    torch.cuda.synchronize()
+    assert fm.check_error() == 0
+    assert_parity(out.numpy(), ref, window_mask(inp["ks"], inp["ke"], 900), True, what="host")
+
+
+# ------------------------------------------------------------------ full-size workloads
+def _sample_rows(M, nrand, seed):
+    rng = np.random.default_rng(seed)
+    rows = set(range(0, min(M, 9))) | set(range(max(0, M - 9), M))
+    rows |= set(rng.choice(M, size=min(M, nrand), replace=False).tolist())
+    return np.array(sorted(rows), np.int64)
+
+
+@pytest.mark.parametrize("name,clean,split_n", [
+    ("causal_8192x8192", True, 0),
+    ("chunk_causal_4096x32768", True, 0),
+    ("chunk_causal_4096x32768", False, 0),
+    ("long_causal_1024x131072", True, 0),
+    ("multi_req_4096x32768", True, 0),
+    ("multi_req_4096x32768", True, 20),
+])
+def test_full_workloads_sampled(name, clean, split_n):
+    wl = workloads.WORKLOADS[name]
+    inp = workloads.make(wl)
+    M, N = inp["M"], inp["N"]
+    dev = to_device(inp)
+    out = poisoned(M, N)
+    fm.fp8_mqa_logits(dev["q"], dev["k"], dev["kv_scale"], dev["w"], dev["ks"], dev["ke"],
+                      out=out, clean_logits=clean, split_n=split_n)
+    assert fm.check_error() == 0
+    # mask on every row: a property that holds at any size
+    bits = out.view(torch.int32)
+    n = torch.arange(N, device="cuda")[None, :]
+    lo = dev["ks"].clamp(0, N).long()[:, None]
+    hi = dev["ke"].clamp(0, N).long()[:, None]
+    inside = (n >= lo) & (n < hi)
+    want_out = int(np.int32(np.uint32(0xFF800000 if clean else 0x7FC0DEAD).view(np.int32)))
+    assert bool(((bits == want_out) | inside).all()), "out-of-window entries wrong"
+    assert bool(torch.isfinite(out)[inside].all()), "non-finite in-window values"
+    # values on sampled rows, element by element
+    rows = _sample_rows(M, 24 if N > 50000 else 48, seed=wl.seed)
+    ref = run_oracle(inp, clean=clean, rows=rows)
+    gpu = out[torch.from_numpy(rows).cuda()].cpu().numpy()
+    assert_parity(gpu, ref, window_mask(inp["ks"], inp["ke"], N, rows), clean,
+                  what=f"{name} clean={clean} split={split_n}")
