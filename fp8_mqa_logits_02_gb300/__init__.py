@@ -58,9 +58,8 @@ class Fp8MqaError(RuntimeError):
 
 def build(force: bool = False, verbose: bool = False) -> str:
     """Compile ``libfp8mqa.so`` in-tree with nvcc for sm_103a."""
-    import importlib
-    builder = importlib.import_module(__name__ + ".build")
-    return builder.build(force=force, verbose=verbose)
+    from . import nvcc_build
+    return nvcc_build.build(force=force, verbose=verbose)
 
 
 def lib():
@@ -71,7 +70,7 @@ def lib():
             if not os.path.exists(LIB_PATH):
                 raise RuntimeError(
                     f"{LIB_PATH} is missing: build it with "
-                    "`python -m fp8_mqa_logits_02_gb300.build` (there is no CPU fallback)")
+                    "`python -m fp8_mqa_logits_02_gb300.nvcc_build` (there is no CPU fallback)")
             handle = ctypes.CDLL(LIB_PATH)
             for name, (res, args) in SIGNATURES.items():
                 fn = getattr(handle, name)

@@ -1,6 +1,6 @@
 """Builds the in-tree CUDA library ``libfp8mqa.so`` for sm_103a with nvcc.
 
-Usage: ``python -m fp8_mqa_logits_02_gb300.build`` (also called by the package's
+Usage: ``python -m fp8_mqa_logits_02_gb300.nvcc_build`` (also called by the package's
 ``build()`` helper).  The output lands next to this file and is git-ignored.
 """
 from __future__ import annotations
