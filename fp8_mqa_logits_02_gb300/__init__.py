@@ -47,6 +47,8 @@ SIGNATURES = {
     "fp8_mqa_logits_host": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I32, _I32,
                                            _I32, _I32, _P, _U64, _P]),
     "fp8_mqa_logits_strerror": (ctypes.c_char_p, [ctypes.c_int]),
+    "fp8_mqa_logits_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I32,
+                                              _I32, _I32, _I32, _P]),
 }
 
 

@@ -217,6 +217,142 @@ int launch(const uint8_t* q, const uint8_t* k, const float* kv, const float* w,
 
 uint64_t align256(uint64_t x) { return (x + 255) & ~uint64_t(255); }
 
+// ---------------------------------------------------------------------------------------
+// Allocation-free variant (fp8_mqa_logits_noalloc).  Its scratch -- the scheduler's work
+// counters and a status word -- lives in the file-scope array below instead of memory
+// from cudaMalloc.  Host code may not pass the array's name to a kernel (on the host it
+// is only a stand-in for the symbol), so set-up looks up its device address once per
+// device with cudaGetSymbolAddress, with that device current.
+constexpr size_t kNoAllocScratchBytes = 256;  // the array's fixed size
+constexpr size_t kNoAllocStatusOffset = 128;  // status word after the scheduler slot
+
+struct NoAllocState {
+    std::once_flag once;
+    int init_status = FP8MQA_OK;
+    int sm_count = 0;
+    uint8_t* scratch = nullptr;  // device address of no_alloc_scratch on this device
+};
+
+NoAllocState g_noalloc[kMaxDevices];
+
+}  // namespace
+}  // namespace fp8mqa
+
+static __device__ __align__(256) uint8_t no_alloc_scratch[fp8mqa::kNoAllocScratchBytes];
+
+namespace fp8mqa {
+namespace {
+
+// Bytes of the array one call uses: a scheduler slot and the status word.  The need does
+// not grow with M or N; the check below guards the layout against the array size.
+constexpr size_t kNoAllocNeed = kNoAllocStatusOffset + sizeof(int32_t);
+static_assert(sizeof(SchedSlot) <= kNoAllocStatusOffset, "scratch layout");
+static_assert(kNoAllocNeed <= kNoAllocScratchBytes, "scratch array too small");
+
+void init_noalloc(int dev, NoAllocState& st)
+{
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&st.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        st.init_status = FP8MQA_ERR_CUDA;
+        return;
+    }
+    if (major != 10 || minor != 3) {
+        st.init_status = FP8MQA_ERR_ARCH;
+        return;
+    }
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, fp8_mqa_logits_kernel) != cudaSuccess ||
+        uint32_t(fa.numRegs) != kLaunchRegs ||
+        cudaFuncSetAttribute(fp8_mqa_logits_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(kSmemBytes)) != cudaSuccess) {
+        st.init_status = FP8MQA_ERR_LAUNCH;
+        return;
+    }
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, no_alloc_scratch) != cudaSuccess || ptr == nullptr) {
+        cudaGetLastError();
+        st.init_status = FP8MQA_ERR_CUDA;
+        return;
+    }
+    st.scratch = static_cast<uint8_t*>(ptr);
+    std::call_once(g_encode_once, load_encode);
+    if (!g_encode) st.init_status = FP8MQA_ERR_CUDA;
+}
+
+int launch_noalloc(const uint8_t* q, const uint8_t* k, const float* kv, const float* w,
+                   const int32_t* ks, const int32_t* ke, float* out, int64_t M, int64_t N,
+                   int32_t clean, int32_t split_n, cudaStream_t stream)
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return FP8MQA_ERR_CUDA;
+    }
+    NoAllocState& st = g_noalloc[dev];
+    std::call_once(st.once, init_noalloc, dev, std::ref(st));
+    if (st.init_status != FP8MQA_OK) return st.init_status;
+    if (kNoAllocNeed > kNoAllocScratchBytes) return FP8MQA_ERR_UNSUPPORTED_SHAPE;
+
+    const int32_t num_tiles = int32_t((N + kTileKeys - 1) / kTileKeys);
+    int32_t split = split_n > 0 ? split_n : fp8_mqa_logits_default_split(M, N, st.sm_count);
+    if (split > num_tiles) split = num_tiles;
+    if (split < 1) split = 1;
+    const int32_t tpc = (num_tiles + split - 1) / split;
+    split = (num_tiles + tpc - 1) / tpc;
+    const int64_t num_blocks = (M + kRows - 1) / kRows;
+    const int64_t num_units = num_blocks * split;
+    if (num_units > INT32_MAX) return FP8MQA_ERR_UNSUPPORTED_SHAPE;
+
+    CUtensorMap maps[4];
+    const cuuint64_t q_dims[2] = {cuuint64_t(kDim), cuuint64_t(M) * kHeads};
+    const cuuint64_t k_dims[2] = {cuuint64_t(kDim), cuuint64_t(N)};
+    const cuuint64_t w_dims[2] = {cuuint64_t(kHeads), cuuint64_t(M)};
+    const cuuint64_t kv_dims[1] = {cuuint64_t(N)};
+    const cuuint64_t row128[1] = {cuuint64_t(kDim)};
+    const cuuint64_t w_stride[1] = {cuuint64_t(kHeads) * 4};
+    const cuuint64_t none[1] = {0};
+    const cuuint32_t q_box[2] = {kDim, kUmmaN};
+    const cuuint32_t k_box[2] = {kDim, kTileKeys};
+    const cuuint32_t w_box[2] = {kHeads, kRows};
+    const cuuint32_t kv_box[1] = {kTileKeys};
+    if (!encode(&maps[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, q, q_dims, row128, q_box,
+                CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode(&maps[1], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, k, k_dims, row128, k_box,
+                CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode(&maps[2], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, w, w_dims, w_stride, w_box,
+                CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode(&maps[3], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 1, kv, kv_dims, none, kv_box,
+                CU_TENSOR_MAP_SWIZZLE_NONE))
+        return FP8MQA_ERR_LAUNCH;
+
+    Params p;
+    p.ks = ks;
+    p.ke = ke;
+    p.out = out;
+    p.M = M;
+    p.N = N;
+    p.num_tiles = num_tiles;
+    p.tiles_per_chunk = tpc;
+    p.split = split;
+    p.num_blocks = int32_t(num_blocks);
+    p.num_units = int32_t(num_units);
+    p.clean = clean;
+    p.sched = reinterpret_cast<SchedSlot*>(st.scratch);
+    p.status = reinterpret_cast<int32_t*>(st.scratch + kNoAllocStatusOffset);
+    p.timeout_ns = kTimeoutNs;
+
+    // The work counters must start at zero; the array keeps whatever the last call left.
+    if (cudaMemsetAsync(st.scratch, 0, sizeof(SchedSlot), stream) != cudaSuccess)
+        return FP8MQA_ERR_CUDA;
+    const int64_t grid = num_units < st.sm_count ? num_units : st.sm_count;
+    fp8_mqa_logits_kernel<<<unsigned(grid), kThreads, kSmemBytes, stream>>>(
+        maps[0], maps[1], maps[2], maps[3], p);
+    if (cudaGetLastError() != cudaSuccess) return FP8MQA_ERR_LAUNCH;
+    return FP8MQA_OK;
+}
+
 }  // namespace
 }  // namespace fp8mqa
 
@@ -327,6 +463,18 @@ int fp8_mqa_logits_host(const uint8_t* q_fp8, const uint8_t* k_fp8, const float*
     if (cudaMemcpyAsync(out, dout, m * n * 4, cudaMemcpyDeviceToHost, s) != cudaSuccess)
         return FP8MQA_ERR_CUDA;
     return FP8MQA_OK;
+}
+
+int fp8_mqa_logits_noalloc(const uint8_t* q_fp8, const uint8_t* k_fp8, const float* kv_scale,
+                           const float* w, const int32_t* ks, const int32_t* ke, float* out,
+                           int64_t M, int64_t N, int32_t H, int32_t D, int32_t clean_logits,
+                           int32_t split_n, void* stream)
+{
+    const int rc = fp8mqa::check_args(q_fp8, k_fp8, kv_scale, w, ks, ke, out, M, N, H, D,
+                                      clean_logits, split_n);
+    if (rc != FP8MQA_OK || M == 0 || N == 0) return rc;
+    return fp8mqa::launch_noalloc(q_fp8, k_fp8, kv_scale, w, ks, ke, out, M, N, clean_logits,
+                                  split_n, static_cast<cudaStream_t>(stream));
 }
 
 const char* fp8_mqa_logits_strerror(int status)

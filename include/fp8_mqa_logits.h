@@ -134,6 +134,36 @@ FP8MQA_API int fp8_mqa_logits_host(const uint8_t* q_fp8, const uint8_t* k_fp8, c
                         int32_t split_n, void* workspace, uint64_t workspace_bytes,
                         void* stream);
 
+/*
+ * fp8_mqa_logits_noalloc -- fp8_mqa_logits for callers that cannot allocate device
+ * memory.  The pages this library follows have no counterpart: it exists for hosts such
+ * as serving engines that reserve nearly all HBM for their own pools up front and forbid
+ * allocations outside them, plug-in interfaces of inference runtimes whose contract bars
+ * a plug-in from allocating, and latency-critical loops where a cudaMalloc (which can
+ * synchronize the device) or a first-call allocation is not acceptable.
+ *
+ * Arguments, layouts, results and errors are those of fp8_mqa_logits; the output is the
+ * same bit for bit.  Differences:
+ *   - It calls no cudaMalloc, cudaFree or other allocating routine.  Its scratch (the
+ *     scheduler's work counters and a status word) is a 256-byte device array compiled
+ *     into the library, which every GPU that loads the library holds until process exit.
+ *     The scratch a call needs does not depend on M or N; a call that needed more than
+ *     the array holds would be refused with FP8MQA_ERR_UNSUPPORTED_SHAPE.
+ *   - The first call on a device looks up the array's device address (once per device,
+ *     with that device current); make that first call before any stream capture.
+ *   - Every call shares the one array.  Each call clears the work counters on `stream`
+ *     before its kernel, so calls that overlap on the GPU (for example on two streams
+ *     at once) race on them and may produce wrong output: order such calls on one
+ *     stream or with events.
+ *   - A bounded on-device wait that gives up is recorded in the array's status word,
+ *     which fp8_mqa_logits_check_error does not read.
+ */
+FP8MQA_API int fp8_mqa_logits_noalloc(const uint8_t* q_fp8, const uint8_t* k_fp8,
+                                      const float* kv_scale, const float* w, const int32_t* ks,
+                                      const int32_t* ke, float* out, int64_t M, int64_t N,
+                                      int32_t H, int32_t D, int32_t clean_logits,
+                                      int32_t split_n, void* stream);
+
 /* fp8_mqa_logits_strerror -- a static, human-readable name for a status code. */
 FP8MQA_API const char* fp8_mqa_logits_strerror(int status);
 
