@@ -140,16 +140,16 @@ int check_args(const uint8_t* q, const uint8_t* k, const float* kv, const float*
     return FP8MQA_OK;
 }
 
-int launch(const uint8_t* q, const uint8_t* k, const float* kv, const float* w,
-           const int32_t* ks, const int32_t* ke, float* out, int64_t M, int64_t N,
-           int32_t clean, int32_t split_n, cudaStream_t stream)
+// Builds the tensor maps and parameters and launches the persistent kernel.  `sched` and
+// `status` are the caller's scratch; with `clear_sched` the scheduler counters are zeroed
+// on `stream` first.
+int enqueue(SchedSlot* sched, int32_t* status, int sm_count, bool clear_sched,
+            const uint8_t* q, const uint8_t* k, const float* kv, const float* w,
+            const int32_t* ks, const int32_t* ke, float* out, int64_t M, int64_t N,
+            int32_t clean, int32_t split_n, cudaStream_t stream)
 {
-    int err = FP8MQA_OK;
-    DeviceState* st = device_state(&err);
-    if (!st) return err;
-
     const int32_t num_tiles = int32_t((N + kTileKeys - 1) / kTileKeys);
-    int32_t split = split_n > 0 ? split_n : fp8_mqa_logits_default_split(M, N, st->sm_count);
+    int32_t split = split_n > 0 ? split_n : fp8_mqa_logits_default_split(M, N, sm_count);
     if (split > num_tiles) split = num_tiles;
     if (split < 1) split = 1;
     const int32_t tpc = (num_tiles + split - 1) / split;
@@ -158,7 +158,7 @@ int launch(const uint8_t* q, const uint8_t* k, const float* kv, const float* w,
     const int64_t num_units = num_blocks * split;
     if (num_units > INT32_MAX) return FP8MQA_ERR_UNSUPPORTED_SHAPE;
 
-    CUtensorMap tm_q, tm_k, tm_w, tm_kv;
+    CUtensorMap tm_q, tm_k, tm_w;
     {
         const cuuint64_t dims[2] = {cuuint64_t(kDim), cuuint64_t(M) * kHeads};
         const cuuint64_t strides[1] = {cuuint64_t(kDim)};
@@ -183,16 +183,8 @@ int launch(const uint8_t* q, const uint8_t* k, const float* kv, const float* w,
                     CU_TENSOR_MAP_SWIZZLE_NONE))
             return FP8MQA_ERR_LAUNCH;
     }
-    {
-        const cuuint64_t dims[1] = {cuuint64_t(N)};
-        const cuuint64_t strides[1] = {0};
-        const cuuint32_t box[1] = {kTileKeys};
-        if (!encode(&tm_kv, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 1, kv, dims, strides, box,
-                    CU_TENSOR_MAP_SWIZZLE_NONE))
-            return FP8MQA_ERR_LAUNCH;
-    }
-
     Params p;
+    p.kv_scale = kv;
     p.ks = ks;
     p.ke = ke;
     p.out = out;
@@ -204,15 +196,28 @@ int launch(const uint8_t* q, const uint8_t* k, const float* kv, const float* w,
     p.num_blocks = int32_t(num_blocks);
     p.num_units = int32_t(num_units);
     p.clean = clean;
-    p.sched = st->sched + (st->seq.fetch_add(1, std::memory_order_relaxed) % kSchedSlots);
-    p.status = st->status;
+    p.sched = sched;
+    p.status = status;
     p.timeout_ns = kTimeoutNs;
 
-    const int64_t grid = num_units < st->sm_count ? num_units : st->sm_count;
-    fp8_mqa_logits_kernel<<<unsigned(grid), kThreads, kSmemBytes, stream>>>(tm_q, tm_k, tm_w,
-                                                                           tm_kv, p);
+    if (clear_sched && cudaMemsetAsync(sched, 0, sizeof(SchedSlot), stream) != cudaSuccess)
+        return FP8MQA_ERR_CUDA;
+    const int64_t grid = num_units < sm_count ? num_units : sm_count;
+    fp8_mqa_logits_kernel<<<unsigned(grid), kThreads, kSmemBytes, stream>>>(tm_q, tm_k, tm_w, p);
     if (cudaGetLastError() != cudaSuccess) return FP8MQA_ERR_LAUNCH;
     return FP8MQA_OK;
+}
+
+int launch(const uint8_t* q, const uint8_t* k, const float* kv, const float* w,
+           const int32_t* ks, const int32_t* ke, float* out, int64_t M, int64_t N,
+           int32_t clean, int32_t split_n, cudaStream_t stream)
+{
+    int err = FP8MQA_OK;
+    DeviceState* st = device_state(&err);
+    if (!st) return err;
+    SchedSlot* slot = st->sched + (st->seq.fetch_add(1, std::memory_order_relaxed) % kSchedSlots);
+    return enqueue(slot, st->status, st->sm_count, false, q, k, kv, w, ks, ke, out, M, N, clean,
+                   split_n, stream);
 }
 
 uint64_t align256(uint64_t x) { return (x + 255) & ~uint64_t(255); }
@@ -294,63 +299,10 @@ int launch_noalloc(const uint8_t* q, const uint8_t* k, const float* kv, const fl
     std::call_once(st.once, init_noalloc, dev, std::ref(st));
     if (st.init_status != FP8MQA_OK) return st.init_status;
     if (kNoAllocNeed > kNoAllocScratchBytes) return FP8MQA_ERR_UNSUPPORTED_SHAPE;
-
-    const int32_t num_tiles = int32_t((N + kTileKeys - 1) / kTileKeys);
-    int32_t split = split_n > 0 ? split_n : fp8_mqa_logits_default_split(M, N, st.sm_count);
-    if (split > num_tiles) split = num_tiles;
-    if (split < 1) split = 1;
-    const int32_t tpc = (num_tiles + split - 1) / split;
-    split = (num_tiles + tpc - 1) / tpc;
-    const int64_t num_blocks = (M + kRows - 1) / kRows;
-    const int64_t num_units = num_blocks * split;
-    if (num_units > INT32_MAX) return FP8MQA_ERR_UNSUPPORTED_SHAPE;
-
-    CUtensorMap maps[4];
-    const cuuint64_t q_dims[2] = {cuuint64_t(kDim), cuuint64_t(M) * kHeads};
-    const cuuint64_t k_dims[2] = {cuuint64_t(kDim), cuuint64_t(N)};
-    const cuuint64_t w_dims[2] = {cuuint64_t(kHeads), cuuint64_t(M)};
-    const cuuint64_t kv_dims[1] = {cuuint64_t(N)};
-    const cuuint64_t row128[1] = {cuuint64_t(kDim)};
-    const cuuint64_t w_stride[1] = {cuuint64_t(kHeads) * 4};
-    const cuuint64_t none[1] = {0};
-    const cuuint32_t q_box[2] = {kDim, kUmmaN};
-    const cuuint32_t k_box[2] = {kDim, kTileKeys};
-    const cuuint32_t w_box[2] = {kHeads, kRows};
-    const cuuint32_t kv_box[1] = {kTileKeys};
-    if (!encode(&maps[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, q, q_dims, row128, q_box,
-                CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode(&maps[1], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, k, k_dims, row128, k_box,
-                CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode(&maps[2], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, w, w_dims, w_stride, w_box,
-                CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !encode(&maps[3], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 1, kv, kv_dims, none, kv_box,
-                CU_TENSOR_MAP_SWIZZLE_NONE))
-        return FP8MQA_ERR_LAUNCH;
-
-    Params p;
-    p.ks = ks;
-    p.ke = ke;
-    p.out = out;
-    p.M = M;
-    p.N = N;
-    p.num_tiles = num_tiles;
-    p.tiles_per_chunk = tpc;
-    p.split = split;
-    p.num_blocks = int32_t(num_blocks);
-    p.num_units = int32_t(num_units);
-    p.clean = clean;
-    p.sched = reinterpret_cast<SchedSlot*>(st.scratch);
-    p.status = reinterpret_cast<int32_t*>(st.scratch + kNoAllocStatusOffset);
-    p.timeout_ns = kTimeoutNs;
-
     // The work counters must start at zero; the array keeps whatever the last call left.
-    if (cudaMemsetAsync(st.scratch, 0, sizeof(SchedSlot), stream) != cudaSuccess)
-        return FP8MQA_ERR_CUDA;
-    const int64_t grid = num_units < st.sm_count ? num_units : st.sm_count;
-    fp8_mqa_logits_kernel<<<unsigned(grid), kThreads, kSmemBytes, stream>>>(
-        maps[0], maps[1], maps[2], maps[3], p);
-    if (cudaGetLastError() != cudaSuccess) return FP8MQA_ERR_LAUNCH;
-    return FP8MQA_OK;
+    return enqueue(reinterpret_cast<SchedSlot*>(st.scratch),
+                   reinterpret_cast<int32_t*>(st.scratch + kNoAllocStatusOffset), st.sm_count,
+                   true, q, k, kv, w, ks, ke, out, M, N, clean, split_n, stream);
 }
 
 }  // namespace

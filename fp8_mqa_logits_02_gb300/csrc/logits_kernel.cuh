@@ -8,11 +8,11 @@
 // CTA per SM pulls units from a global counter, heaviest row blocks first (the page's
 // "reverse_rows", section "Design / Grid choice"); key chunks are the page's SplitN.
 //
-// Warp roles in a 384-thread CTA:
+// Warp roles in a 640-thread CTA:
 //   warp 0      producer: claims units, computes each unit's key-tile range from the
-//               window union of its rows, and streams Q+w (once per unit) and K+kv_scale
-//               tiles (once per unit) into shared memory with TMA (page: "K is read once
-//               per 32 rows" and "kv_scale is staged next to it", section "Design").
+//               window union of its rows, and streams Q+w (once per unit) and K tiles
+//               (once per unit) into shared memory with TMA (page: "K is read once per 32
+//               rows", section "Design").
 //   warp 1      TMEM owner and MMA issuer: per 128-key tile, 4 tcgen05.mma (K = 32 each)
 //               of A = K tile [128 keys x 128] by B = Q block [8 rows x 32 heads = 256 x
 //               128], accumulating S[key, (row, head)] in fp32 in one of two TMEM buffers.
@@ -20,11 +20,13 @@
 //               computed tile range, on their own light-first unit order so the writes
 //               overlap the compute-heavy units (page: "With clean_logits the kernel writes
 //               -inf itself").
-//   warps 4-11  epilogue: thread = one key (TMEM lane), so one tcgen05.ld gives it the 32
-//               heads of one query row; relu, times w, head sum in registers (no cross-lane
+//   warps 4-19  epilogue, four warps per SM sub-partition, two query rows per warp:
+//               thread = one key (TMEM lane), so one tcgen05.ld gives it the 32 heads of
+//               one query row; relu, times w, head sum in registers (no cross-lane
 //               reduction), times kv_scale once per (m, n), then a coalesced store.  Tiles
-//               fully inside every row's window store without compare/select; boundary
-//               tiles are masked (page: "clean stages" vs "masked boundary stages").
+//               inside both rows' windows store without compare/select; boundary tiles are
+//               masked (page: "clean stages" vs "masked boundary stages").  kv_scale comes
+//               through the read-only data path, fetched one tile ahead.
 //
 // Keys sit on the MMA M axis (TMEM lanes) and (row, head) on the N axis: this transposes
 // the page's layout (query heads on the matrix rows) so that the head reduction is a sum
@@ -48,29 +50,26 @@ constexpr int kRows = 8;                  // query rows per unit
 constexpr int kTileKeys = 128;            // keys per tile (MMA M)
 constexpr int kUmmaN = kRows * kHeads;    // 256 (MMA N)
 constexpr int kUmmaK = 32;                // FP8 K per tcgen05.mma
-constexpr int kStages = 6;                // K / kv_scale ring depth
-constexpr int kQSlots = 2;
+constexpr int kStages = 6;                // K ring depth
+constexpr int kQSlots = 3;
 constexpr int kUnitSlots = 4;
 constexpr int kAccBufs = 2;
 constexpr uint32_t kTmemCols = kAccBufs * kUmmaN;  // 512
-constexpr int kThreads = 384;
 constexpr int kEpiWarp0 = 4;
-constexpr int kEpiWarps = 8;
-constexpr int kRowsPerEpiWarp = 4;
+constexpr int kEpiWarps = 16;
+constexpr int kThreads = (kEpiWarp0 + kEpiWarps) * 32;  // 640
+constexpr int kRowsPerEpiWarp = kRows * 4 / kEpiWarps;   // 2 (4 sub-partitions)
 constexpr int kFillWarp0 = 2;
-constexpr int kFillWarps = 2;
 
 constexpr uint32_t kQBytes = kRows * kHeads * kDim;   // 32768
 constexpr uint32_t kWBytes = kRows * kHeads * 4;      // 1024
 constexpr uint32_t kKBytes = kTileKeys * kDim;        // 16384
-constexpr uint32_t kKvBytes = kTileKeys * 4;          // 512
 
 // Shared-memory layout, offsets from a 1024-byte aligned base.
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffK = kOffQ + kQSlots * kQBytes;
 constexpr uint32_t kOffW = kOffK + kStages * kKBytes;
-constexpr uint32_t kOffKv = kOffW + kQSlots * kWBytes;
-constexpr uint32_t kOffBar = kOffKv + kStages * kKvBytes;
+constexpr uint32_t kOffBar = kOffW + kQSlots * kWBytes;
 
 constexpr int kBarKFull = 0;
 constexpr int kBarKEmpty = kBarKFull + kStages;
@@ -95,13 +94,15 @@ constexpr uint32_t kOffMisc = kOffUnits + kUnitSlots * sizeof(UnitInfo);
 constexpr uint32_t kSmemUsed = kOffMisc + 16;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // slack for aligning the base
 static_assert(kSmemBytes <= 232448, "shared memory budget");
+static_assert(kRowsPerEpiWarp == 2, "the epilogue is written for two rows per warp");
 
 // Per-role register budgets (setmaxnreg); the sum must equal the launch allocation
-// 384 threads x 168 registers.
-constexpr uint32_t kLaunchRegs = 168;
-constexpr uint32_t kCtlRegs = 56;
-constexpr uint32_t kEpiRegs = 224;
-static_assert(128 * kCtlRegs + 256 * kEpiRegs <= kThreads * kLaunchRegs, "register split");
+// 640 threads x 96 registers.
+constexpr uint32_t kLaunchRegs = 96;
+constexpr uint32_t kCtlRegs = 32;
+constexpr uint32_t kEpiRegs = 112;
+static_assert(128 * kCtlRegs + kEpiWarps * 32 * kEpiRegs == kThreads * kLaunchRegs,
+              "register split");
 
 // Status word bits.
 constexpr int32_t kStatusTimeout = 1;
@@ -115,6 +116,7 @@ struct SchedSlot {
 };
 
 struct Params {
+    const float* kv_scale;
     const int32_t* ks;
     const int32_t* ke;
     float* out;
@@ -185,6 +187,16 @@ __device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity, con
         }
     }
     return ok != 0;
+}
+
+// Bounded wait by lane 0 only, result broadcast to the warp.  For barriers whose data the
+// warp reads through tcgen05 (ordered by tcgen05.fence::after_thread_sync), not through
+// generic loads.
+__device__ __forceinline__ bool wait_bar_lane0(uint32_t bar, uint32_t parity, const Ctl& c)
+{
+    int ok = 1;
+    if ((threadIdx.x & 31) == 0) ok = wait_bar(bar, parity, c) ? 1 : 0;
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
 // Drain: wait for a phase without looking at the abort flag (still time-bounded).
@@ -262,36 +274,33 @@ __device__ __forceinline__ void fill_neg_inf(float* row, int64_t a, int64_t e)
     if (lane < e - a) __stcs(row + a + lane, ninf);
 }
 
-__device__ __forceinline__ float relu_dot_row(const uint32_t* s, const float2* w2)
+__device__ __forceinline__ float2 relu2(uint32_t a, uint32_t b)
 {
-    // sum_h max(s_h, 0) * w_h with four independent fp32x2 accumulators
-    float2 a0 = make_float2(0.f, 0.f), a1 = a0, a2 = a0, a3 = a0;
+    return make_float2(fmaxf(__uint_as_float(a), 0.f), fmaxf(__uint_as_float(b), 0.f));
+}
+
+// a[c] += max(s_h, 0) * w_h over 16 heads (w points at their 8 weight pairs), spread over
+// four fp32x2 accumulator chains.
+__device__ __forceinline__ void relu_acc16(const uint32_t (&s)[16], const float2* w, float2 (&a)[4])
+{
 #pragma unroll
-    for (int h = 0; h < kHeads; h += 8) {
-        a0 = __ffma2_rn(make_float2(fmaxf(__uint_as_float(s[h + 0]), 0.f),
-                                    fmaxf(__uint_as_float(s[h + 1]), 0.f)),
-                        w2[(h >> 1) + 0], a0);
-        a1 = __ffma2_rn(make_float2(fmaxf(__uint_as_float(s[h + 2]), 0.f),
-                                    fmaxf(__uint_as_float(s[h + 3]), 0.f)),
-                        w2[(h >> 1) + 1], a1);
-        a2 = __ffma2_rn(make_float2(fmaxf(__uint_as_float(s[h + 4]), 0.f),
-                                    fmaxf(__uint_as_float(s[h + 5]), 0.f)),
-                        w2[(h >> 1) + 2], a2);
-        a3 = __ffma2_rn(make_float2(fmaxf(__uint_as_float(s[h + 6]), 0.f),
-                                    fmaxf(__uint_as_float(s[h + 7]), 0.f)),
-                        w2[(h >> 1) + 3], a3);
+    for (int h = 0; h < 16; h += 8) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+            a[c] = __ffma2_rn(relu2(s[h + 2 * c], s[h + 2 * c + 1]), w[(h >> 1) + c], a[c]);
     }
-    const float2 b0 = __fadd2_rn(a0, a1);
-    const float2 b1 = __fadd2_rn(a2, a3);
-    const float2 c0 = __fadd2_rn(b0, b1);
-    return c0.x + c0.y;
+}
+
+__device__ __forceinline__ float sum4(const float2 (&a)[4])
+{
+    const float2 r = __fadd2_rn(__fadd2_rn(a[0], a[1]), __fadd2_rn(a[2], a[3]));
+    return r.x + r.y;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
     fp8_mqa_logits_kernel(const __grid_constant__ CUtensorMap tm_q,
                           const __grid_constant__ CUtensorMap tm_k,
-                          const __grid_constant__ CUtensorMap tm_w,
-                          const __grid_constant__ CUtensorMap tm_kv, const Params p)
+                          const __grid_constant__ CUtensorMap tm_w, const Params p)
 {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_base = ptx::smem_addr(smem_raw);
@@ -311,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
             ptx::mbar_init(bar(kBarKFull + i), 1);
-            ptx::mbar_init(bar(kBarKEmpty + i), 1 + kEpiWarps);
+            ptx::mbar_init(bar(kBarKEmpty + i), 1);
         }
         for (int i = 0; i < kQSlots; ++i) {
             ptx::mbar_init(bar(kBarQFull + i), 1);
@@ -333,7 +342,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::prefetch_tensormap(&tm_q);
         ptx::prefetch_tensormap(&tm_k);
         ptx::prefetch_tensormap(&tm_w);
-        ptx::prefetch_tensormap(&tm_kv);
     }
     if (warp == 1) {
         ptx::tmem_alloc(sbase + kOffMisc, kTmemCols);
@@ -395,11 +403,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = wait_bar(bar(kBarKEmpty + st), ((g / kStages) & 1u) ^ 1u, ctl);
                         if (!ok) break;
                         const uint32_t fb = bar(kBarKFull + st);
-                        ptx::mbar_arrive_expect_tx(fb, kKBytes + kKvBytes);
+                        ptx::mbar_arrive_expect_tx(fb, kKBytes);
                         ptx::tma_load_2d_hint(sbase + kOffK + st * kKBytes, &tm_k, fb, 0,
                                               t * kTileKeys, pol_k);
-                        ptx::tma_load_1d(sbase + kOffKv + st * kKvBytes, &tm_kv, fb,
-                                         t * kTileKeys);
                         ++g;
                     }
                 }
@@ -498,12 +504,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ------------------------------------------------------------ epilogue
         ptx::regs_inc<kEpiRegs>();
-        const int sp = warp & 3;                          // TMEM sub-partition
-        const int half = (warp - kEpiWarp0) >> 2;        // which 4 of the 8 rows
+        const int sp = warp & 3;                                // TMEM sub-partition
+        const int quarter = (warp - kEpiWarp0) >> 2;           // which 2 of the 8 rows
         const uint32_t lane_base = uint32_t(sp * 32) << 16;
         const float ninf = __int_as_float(0xff800000u);
+        const int32_t N = int32_t(p.N);
         uint32_t ui = 0, g = 0, qi = 0;
-        float2 w2[kRowsPerEpiWarp][kHeads / 2];
+        float2 wa[kHeads / 2], wb[kHeads / 2];
         bool ok = true;
         while (ok) {
             const uint32_t slot = ui % kUnitSlots;
@@ -520,78 +527,101 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++qi;
             {
                 const float4* wsrc = reinterpret_cast<const float4*>(
-                    smem + kOffW + qs * kWBytes + half * kRowsPerEpiWarp * kHeads * 4);
+                    smem + kOffW + qs * kWBytes + quarter * kRowsPerEpiWarp * kHeads * 4);
 #pragma unroll
-                for (int r = 0; r < kRowsPerEpiWarp; ++r) {
-#pragma unroll
-                    for (int j = 0; j < kHeads / 4; ++j) {
-                        const float4 v = wsrc[r * (kHeads / 4) + j];
-                        w2[r][2 * j] = make_float2(v.x, v.y);
-                        w2[r][2 * j + 1] = make_float2(v.z, v.w);
-                    }
+                for (int j = 0; j < kHeads / 4; ++j) {
+                    const float4 x = wsrc[j];
+                    const float4 y = wsrc[kHeads / 4 + j];
+                    wa[2 * j] = make_float2(x.x, x.y);
+                    wa[2 * j + 1] = make_float2(x.z, x.w);
+                    wb[2 * j] = make_float2(y.x, y.y);
+                    wb[2 * j + 1] = make_float2(y.z, y.w);
                 }
             }
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(bar(kBarQEmpty + qs));
 
-            int64_t rlo[kRowsPerEpiWarp], rhi[kRowsPerEpiWarp];
-            bool rok[kRowsPerEpiWarp];
-#pragma unroll
-            for (int r = 0; r < kRowsPerEpiWarp; ++r) {
-                const int64_t m = int64_t(info.m0) + half * kRowsPerEpiWarp + r;
-                rok[r] = m < p.M;
-                rlo[r] = rok[r] ? clamp64(p.ks[m], 0, p.N) : 0;
-                rhi[r] = rok[r] ? clamp64(p.ke[m], 0, p.N) : 0;
+            // This warp's two rows: clamped windows, output rows, and the key tiles that lie
+            // inside both windows (stored without compare/select).
+            const int64_t ma = int64_t(info.m0) + quarter * kRowsPerEpiWarp;
+            const bool oka = ma < p.M, okb = ma + 1 < p.M;
+            const int32_t loa = oka ? int32_t(clamp64(p.ks[ma], 0, p.N)) : 0;
+            const int32_t hia = oka ? int32_t(clamp64(p.ke[ma], 0, p.N)) : 0;
+            const int32_t lob = okb ? int32_t(clamp64(p.ks[ma + 1], 0, p.N)) : 0;
+            const int32_t hib = okb ? int32_t(clamp64(p.ke[ma + 1], 0, p.N)) : 0;
+            int32_t tcl = 0, tch = oka ? INT32_MAX : 0;
+            if (oka) {
+                tcl = max(tcl, (loa + kTileKeys - 1) / kTileKeys);
+                tch = min(tch, hia / kTileKeys);
             }
+            if (okb) {
+                tcl = max(tcl, (lob + kTileKeys - 1) / kTileKeys);
+                tch = min(tch, hib / kTileKeys);
+            } else {
+                tch = 0;  // a missing second row takes the masked path
+            }
+            float* rowa = p.out + ma * p.N;
+            float* rowb = rowa + p.N;
 
-            for (int32_t t = info.t0; t < info.t1; ++t) {
-                const uint32_t st = g % kStages;
+            int32_t n = info.t0 * kTileKeys + sp * 32 + lane;
+            float kv_next = n < N ? __ldg(p.kv_scale + n) : 0.f;
+            for (int32_t t = info.t0; t < info.t1; ++t, n += kTileKeys) {
+                const float kv = kv_next;
+                if (t + 1 < info.t1 && n + kTileKeys < N) kv_next = __ldg(p.kv_scale + n + kTileKeys);
                 const uint32_t ab = g & 1u;
-                if (!wait_bar_warp(bar(kBarKFull + st), (g / kStages) & 1u, ctl)) {
-                    ok = false;
-                    break;
-                }
-                const float kv = reinterpret_cast<const float*>(
-                    smem + kOffKv + st * kKvBytes)[sp * 32 + lane];
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(bar(kBarKEmpty + st));
-                if (!wait_bar_warp(bar(kBarAccFull + ab), (g >> 1) & 1u, ctl)) {
+                if (!wait_bar_lane0(bar(kBarAccFull + ab), (g >> 1) & 1u, ctl)) {
                     ok = false;
                     break;
                 }
                 ptx::tc_fence_after();
-
-                const int64_t n0 = int64_t(t) * kTileKeys;
-                const int64_t n = n0 + sp * 32 + lane;
-                const uint32_t taddr =
-                    tmem_base + lane_base + ab * kUmmaN + uint32_t(half * kRowsPerEpiWarp * kHeads);
-                float v[kRowsPerEpiWarp];
+                const uint32_t taddr = tmem_base + lane_base + ab * kUmmaN +
+                                       uint32_t(quarter * kRowsPerEpiWarp * kHeads);
+                // sum_h relu(S[n, (m, h)]) * w[m, h] for the two rows, 16 heads per TMEM load
+                float va, vb;
+                {
+                    uint32_t s[16];
+                    float2 a[4];
 #pragma unroll
-                for (int r = 0; r < kRowsPerEpiWarp; ++r) {
-                    uint32_t s[32];
-                    ptx::tmem_ld_32x32b_x32(taddr + uint32_t(r * kHeads), s);
-                    ptx::tmem_wait_ld();
-                    if (r == kRowsPerEpiWarp - 1) {
-                        // all of this warp's accumulator reads are done: release the buffer
-                        ptx::tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) ptx::mbar_arrive(bar(kBarAccEmpty + ab));
-                    }
-                    v[r] = relu_dot_row(s, w2[r]) * kv;
+                    for (int c = 0; c < 4; ++c) a[c] = make_float2(0.f, 0.f);
+                    ptx::tmem_ld_32x32b_x16(taddr, s);
+                    ptx::tmem_wait_ld_regs16(s);
+                    relu_acc16(s, wa, a);
+                    ptx::tmem_ld_32x32b_x16(taddr + 16, s);
+                    ptx::tmem_wait_ld_regs16(s);
+                    relu_acc16(s, wa + 8, a);
+                    va = sum4(a);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) a[c] = make_float2(0.f, 0.f);
+                    ptx::tmem_ld_32x32b_x16(taddr + kHeads, s);
+                    ptx::tmem_wait_ld_regs16(s);
+                    relu_acc16(s, wb, a);
+                    ptx::tmem_ld_32x32b_x16(taddr + kHeads + 16, s);
+                    ptx::tmem_wait_ld_regs16(s);
+                    // this warp's accumulator reads are done: release the buffer
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(bar(kBarAccEmpty + ab));
+                    relu_acc16(s, wb + 8, a);
+                    vb = sum4(a);
                 }
-#pragma unroll
-                for (int r = 0; r < kRowsPerEpiWarp; ++r) {
-                    if (!rok[r]) continue;
-                    float* dst = p.out + (int64_t(info.m0) + half * kRowsPerEpiWarp + r) * p.N;
-                    const bool full = n0 >= rlo[r] && n0 + kTileKeys <= rhi[r];
-                    if (full) {
-                        __stcs(dst + n, v[r]);  // clean tile: no compare/select
-                    } else if (n < p.N) {
-                        const bool inside = n >= rlo[r] && n < rhi[r];
-                        if (inside)
-                            __stcs(dst + n, v[r]);
+                va *= kv;
+                vb *= kv;
+                if (t >= tcl && t < tch) {
+                    // clean tile: inside both windows, so n < N and both rows exist
+                    __stcs(rowa + n, va);
+                    __stcs(rowb + n, vb);
+                } else if (n < N) {
+                    if (oka) {
+                        if (n >= loa && n < hia)
+                            __stcs(rowa + n, va);
                         else if (p.clean)
-                            __stcs(dst + n, ninf);
+                            __stcs(rowa + n, ninf);
+                    }
+                    if (okb) {
+                        if (n >= lob && n < hib)
+                            __stcs(rowb + n, vb);
+                        else if (p.clean)
+                            __stcs(rowb + n, ninf);
                     }
                 }
                 ++g;
