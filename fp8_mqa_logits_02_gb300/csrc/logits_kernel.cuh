@@ -13,11 +13,12 @@
 //               window union of its rows, and streams Q+w (once per unit) and K tiles
 //               (once per unit) into shared memory with TMA (page: "K is read once per 32
 //               rows", section "Design").
-//   warp 1      TMEM owner and MMA issuer: per 128-key tile, 4 tcgen05.mma (K = 32 each)
-//               of A = K tile [128 keys x 128] by B = Q block [8 rows x 32 heads = 256 x
-//               128], accumulating S[key, (row, head)] in fp32 in one of two TMEM buffers.
-//   warps 2-3   -inf writers (clean_logits = 1): fill every out-of-window span outside the
-//               computed tile range, on their own light-first unit order so the writes
+//   warps 1, 3  MMA issuers (warp 1 also owns TMEM): per 128-key tile, 4 tcgen05.mma (K = 32
+//               each) of A = K tile [128 keys x 128] by B = Q block [8 rows x 32 heads =
+//               256 x 128], accumulating S[key, (row, head)] in fp32 in TMEM; warp 1 issues
+//               the even tiles into buffer 0, warp 3 the odd tiles into buffer 1.
+//   warp 2      -inf writer (clean_logits = 1): fills every out-of-window span outside the
+//               computed tile range, on its own light-first unit order so the writes
 //               overlap the compute-heavy units (page: "With clean_logits the kernel writes
 //               -inf itself").
 //   warps 4-19  epilogue, four warps per SM sub-partition, two query rows per warp:
@@ -55,11 +56,18 @@ constexpr int kQSlots = 3;
 constexpr int kUnitSlots = 4;
 constexpr int kAccBufs = 2;
 constexpr uint32_t kTmemCols = kAccBufs * kUmmaN;  // 512
+// Query rows each epilogue warp reduces per tile (2 or 4): more rows per warp amortise the
+// per-tile synchronisation over more arithmetic, fewer rows give more warps per SM.
+#ifndef FP8MQA_ROWS_PER_WARP
+#define FP8MQA_ROWS_PER_WARP 2
+#endif
+constexpr int kRowsPerEpiWarp = FP8MQA_ROWS_PER_WARP;
 constexpr int kEpiWarp0 = 4;
-constexpr int kEpiWarps = 16;
-constexpr int kThreads = (kEpiWarp0 + kEpiWarps) * 32;  // 640
-constexpr int kRowsPerEpiWarp = kRows * 4 / kEpiWarps;   // 2 (4 sub-partitions)
-constexpr int kFillWarp0 = 2;
+constexpr int kEpiWarps = kRows * 4 / kRowsPerEpiWarp;  // 4 TMEM sub-partitions
+constexpr int kThreads = (kEpiWarp0 + kEpiWarps) * 32;
+constexpr int kMmaWarp0 = 1;              // issues the even tiles (accumulator buffer 0)
+constexpr int kMmaWarp1 = 3;              // issues the odd tiles (accumulator buffer 1)
+constexpr int kFillWarp = 2;
 
 constexpr uint32_t kQBytes = kRows * kHeads * kDim;   // 32768
 constexpr uint32_t kWBytes = kRows * kHeads * 4;      // 1024
@@ -94,14 +102,15 @@ constexpr uint32_t kOffMisc = kOffUnits + kUnitSlots * sizeof(UnitInfo);
 constexpr uint32_t kSmemUsed = kOffMisc + 16;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // slack for aligning the base
 static_assert(kSmemBytes <= 232448, "shared memory budget");
-static_assert(kRowsPerEpiWarp == 2, "the epilogue is written for two rows per warp");
+static_assert(kRowsPerEpiWarp == 2 || kRowsPerEpiWarp == 4, "two or four rows per warp");
 
-// Per-role register budgets (setmaxnreg); the sum must equal the launch allocation
-// 640 threads x 96 registers.
-constexpr uint32_t kLaunchRegs = 96;
-constexpr uint32_t kCtlRegs = 32;
-constexpr uint32_t kEpiRegs = 112;
-static_assert(128 * kCtlRegs + kEpiWarps * 32 * kEpiRegs == kThreads * kLaunchRegs,
+// Per-role register budgets (setmaxnreg): the control warpgroup gives registers to the
+// epilogue warpgroups; the total must stay within the launch allocation (threads x the
+// per-thread count the kernel is compiled to, which fills the register file).
+constexpr uint32_t kLaunchRegs = (65536u / kThreads) & ~7u;  // 168 or 96
+constexpr uint32_t kCtlRegs = kRowsPerEpiWarp == 4 ? 56u : 32u;
+constexpr uint32_t kEpiRegs = ((kLaunchRegs * kThreads - 128u * kCtlRegs) / (kEpiWarps * 32u)) & ~7u;
+static_assert(128 * kCtlRegs + kEpiWarps * 32 * kEpiRegs <= kThreads * kLaunchRegs,
               "register split");
 
 // Status word bits.
@@ -164,7 +173,8 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Ct
     if (ptx::mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = ptx::globaltimer_ns();
     while (true) {
-        if (ptx::mbar_try_wait(bar, parity)) return true;
+        // sleep until the phase completes (or 20 us pass), then re-check abort and timeout
+        if (ptx::mbar_try_wait_sleep(bar, parity, 20000u)) return true;
         if (*c.abort) return false;
         if (ptx::globaltimer_ns() - t0 > c.timeout_ns) {
             *c.abort = 1;
@@ -197,6 +207,25 @@ __device__ __forceinline__ bool wait_bar_lane0(uint32_t bar, uint32_t parity, co
     int ok = 1;
     if ((threadIdx.x & 31) == 0) ok = wait_bar(bar, parity, c) ? 1 : 0;
     return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+// Bounded wait by every lane of a warp, without lane-0 branches: all lanes poll and a warp
+// vote decides, so the warp stays converged.  Returns false (for the whole warp) when the
+// CTA is aborting or the wait timed out.
+__device__ __forceinline__ bool wait_bar_all(uint32_t bar, uint32_t parity, const Ctl& c)
+{
+    if (__all_sync(0xffffffffu, ptx::mbar_try_wait(bar, parity))) return true;
+    const uint64_t t0 = ptx::globaltimer_ns();
+    while (true) {
+        if (__all_sync(0xffffffffu, ptx::mbar_try_wait_sleep(bar, parity, 20000u))) return true;
+        int stop = *c.abort ? 1 : 0;
+        if ((threadIdx.x & 31) == 0 && !stop && ptx::globaltimer_ns() - t0 > c.timeout_ns) {
+            *c.abort = 1;
+            atomicOr(c.status, kStatusTimeout);
+            stop = 1;
+        }
+        if (__any_sync(0xffffffffu, stop)) return false;
+    }
 }
 
 // Drain: wait for a phase without looking at the abort flag (still time-bounded).
@@ -279,16 +308,90 @@ __device__ __forceinline__ float2 relu2(uint32_t a, uint32_t b)
     return make_float2(fmaxf(__uint_as_float(a), 0.f), fmaxf(__uint_as_float(b), 0.f));
 }
 
-// a[c] += max(s_h, 0) * w_h over 16 heads (w points at their 8 weight pairs), spread over
-// four fp32x2 accumulator chains.
-__device__ __forceinline__ void relu_acc16(const uint32_t (&s)[16], const float2* w, float2 (&a)[4])
+// Head quads (4 heads) whose relu runs on the FMA pipe instead of the ALU: for those the
+// sum takes s*w + |s|*w = 2 relu(s) w, in separate chains halved at the end.  Splitting the
+// relu between the ALU (max, half rate) and the FMA pipe (|x| operands are free) balances
+// the two pipes.  Any mask is valid; the default was chosen by measurement.
+#ifndef FP8MQA_ABS_QUADS
+#define FP8MQA_ABS_QUADS 0xA4u
+#endif
+constexpr uint32_t kAbsQuads = FP8MQA_ABS_QUADS;
+
+__device__ __forceinline__ float2 abs2(float2 v) { return make_float2(fabsf(v.x), fabsf(v.y)); }
+
+// sum_h relu(S[h]) * w[h] for two query rows: s[0..31] row a, s[32..63] row b; w of row a in
+// wsm[0..7] and of row b in wsm[8..15] (shared memory, 4 heads per float4).
+__device__ __forceinline__ void relu_dot_2rows(const uint32_t (&s)[64], const float4* wsm,
+                                               float& va, float& vb)
 {
+    constexpr bool kAnyMax = (kAbsQuads & 0xFFu) != 0xFFu;
+    constexpr bool kAnyAbs = (kAbsQuads & 0xFFu) != 0u;
+    float2 a[4], b[4], ca[2], cb[2];
+    bool a_init[4] = {false, false, false, false}, c_init = false;
 #pragma unroll
-    for (int h = 0; h < 16; h += 8) {
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-            a[c] = __ffma2_rn(relu2(s[h + 2 * c], s[h + 2 * c + 1]), w[(h >> 1) + c], a[c]);
+    for (int j = 0; j < kHeads / 4; ++j) {
+        const float4 x = wsm[j];
+        const float4 y = wsm[kHeads / 4 + j];
+        const float2 wa0 = make_float2(x.x, x.y), wa1 = make_float2(x.z, x.w);
+        const float2 wb0 = make_float2(y.x, y.y), wb1 = make_float2(y.z, y.w);
+        const float2 sa0 = make_float2(__uint_as_float(s[4 * j]), __uint_as_float(s[4 * j + 1]));
+        const float2 sa1 = make_float2(__uint_as_float(s[4 * j + 2]), __uint_as_float(s[4 * j + 3]));
+        const float2 sb0 = make_float2(__uint_as_float(s[32 + 4 * j]), __uint_as_float(s[32 + 4 * j + 1]));
+        const float2 sb1 = make_float2(__uint_as_float(s[32 + 4 * j + 2]), __uint_as_float(s[32 + 4 * j + 3]));
+        if (kAbsQuads & (1u << j)) {
+            if (!c_init) {
+                ca[0] = __fmul2_rn(sa0, wa0);
+                cb[0] = __fmul2_rn(sb0, wb0);
+                ca[1] = __fmul2_rn(sa1, wa1);
+                cb[1] = __fmul2_rn(sb1, wb1);
+                c_init = true;
+            } else {
+                ca[0] = __ffma2_rn(sa0, wa0, ca[0]);
+                cb[0] = __ffma2_rn(sb0, wb0, cb[0]);
+                ca[1] = __ffma2_rn(sa1, wa1, ca[1]);
+                cb[1] = __ffma2_rn(sb1, wb1, cb[1]);
+            }
+            ca[0] = __ffma2_rn(abs2(sa0), wa0, ca[0]);
+            cb[0] = __ffma2_rn(abs2(sb0), wb0, cb[0]);
+            ca[1] = __ffma2_rn(abs2(sa1), wa1, ca[1]);
+            cb[1] = __ffma2_rn(abs2(sb1), wb1, cb[1]);
+        } else {
+            const int c = (2 * j) & 3;
+            const float2 ra0 = make_float2(fmaxf(sa0.x, 0.f), fmaxf(sa0.y, 0.f));
+            const float2 ra1 = make_float2(fmaxf(sa1.x, 0.f), fmaxf(sa1.y, 0.f));
+            const float2 rb0 = make_float2(fmaxf(sb0.x, 0.f), fmaxf(sb0.y, 0.f));
+            const float2 rb1 = make_float2(fmaxf(sb1.x, 0.f), fmaxf(sb1.y, 0.f));
+            if (!a_init[c]) {
+                a[c] = __fmul2_rn(ra0, wa0);
+                a[c + 1] = __fmul2_rn(ra1, wa1);
+                b[c] = __fmul2_rn(rb0, wb0);
+                b[c + 1] = __fmul2_rn(rb1, wb1);
+                a_init[c] = a_init[c + 1] = true;
+            } else {
+                a[c] = __ffma2_rn(ra0, wa0, a[c]);
+                a[c + 1] = __ffma2_rn(ra1, wa1, a[c + 1]);
+                b[c] = __ffma2_rn(rb0, wb0, b[c]);
+                b[c + 1] = __ffma2_rn(rb1, wb1, b[c + 1]);
+            }
+        }
     }
+    float2 ra = make_float2(0.f, 0.f), rb = ra;
+    if (kAnyMax) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            if (a_init[c]) {
+                ra = __fadd2_rn(ra, a[c]);
+                rb = __fadd2_rn(rb, b[c]);
+            }
+        }
+    }
+    if (kAnyAbs) {
+        const float2 half = make_float2(0.5f, 0.5f);
+        ra = __ffma2_rn(__fadd2_rn(ca[0], ca[1]), half, ra);
+        rb = __ffma2_rn(__fadd2_rn(cb[0], cb[1]), half, rb);
+    }
+    va = ra.x + ra.y;
+    vb = rb.x + rb.y;
 }
 
 __device__ __forceinline__ float sum4(const float2 (&a)[4])
@@ -324,17 +427,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < kQSlots; ++i) {
             ptx::mbar_init(bar(kBarQFull + i), 1);
-            ptx::mbar_init(bar(kBarQEmpty + i), 1 + kEpiWarps);
+            ptx::mbar_init(bar(kBarQEmpty + i), 2 + kEpiWarps);
         }
         for (int i = 0; i < kAccBufs; ++i) {
             ptx::mbar_init(bar(kBarAccFull + i), 1);
-            ptx::mbar_init(bar(kBarAccEmpty + i), kEpiWarps);
+            ptx::mbar_init(bar(kBarAccEmpty + i), kEpiWarps * 32);  // every epilogue lane
         }
         for (int i = 0; i < kUnitSlots; ++i) {
             ptx::mbar_init(bar(kBarUnitFull + i), 1);
-            ptx::mbar_init(bar(kBarUnitEmpty + i), 1 + kEpiWarps);
+            ptx::mbar_init(bar(kBarUnitEmpty + i), 2 + kEpiWarps);
         }
-        ptx::mbar_init(bar(kBarDrain), 1);
+        ptx::mbar_init(bar(kBarDrain), 2);
         *abort_flag = 0;
         ptx::mbar_init_fence();
     }
@@ -343,7 +446,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::prefetch_tensormap(&tm_k);
         ptx::prefetch_tensormap(&tm_w);
     }
-    if (warp == 1) {
+    if (warp == kMmaWarp0) {
         ptx::tmem_alloc(sbase + kOffMisc, kTmemCols);
         ptx::tmem_relinquish();
     }
@@ -422,9 +525,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (uint32_t j = (qi > kQSlots ? qi - kQSlots : 0); j < qi; ++j)
                 drain_bar(bar(kBarQFull + j % kQSlots), (j / kQSlots) & 1u, p.timeout_ns);
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
+    } else if (warp == kMmaWarp0 || warp == kMmaWarp1) {
+        // ------------------------------------------------------------ MMA issuers
+        // Two issuers on different SM sub-partitions take alternate tiles, so each owns one
+        // accumulator buffer; issuing tcgen05.mma slows the issuing sub-partition's other
+        // warps, and splitting it keeps any one set of epilogue warps from falling behind.
         if (lane == 0) {
+            const uint32_t par = warp == kMmaWarp1 ? 1u : 0u;
             uint32_t ui = 0, g = 0, qi = 0;
             bool ok = true;
             while (ok) {
@@ -442,6 +549,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int32_t t = info.t0; t < info.t1; ++t) {
                     const uint32_t st = g % kStages;
                     const uint32_t ab = g & 1u;
+                    if (ab != par) {  // the other issuer's tile
+                        ++g;
+                        continue;
+                    }
                     if (!wait_bar(bar(kBarKFull + st), (g / kStages) & 1u, ctl)) {
                         ok = false;
                         break;
@@ -504,13 +615,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ------------------------------------------------------------ epilogue
         ptx::regs_inc<kEpiRegs>();
+        constexpr int kPairs = kRowsPerEpiWarp / 2;
         const int sp = warp & 3;                                // TMEM sub-partition
-        const int quarter = (warp - kEpiWarp0) >> 2;           // which 2 of the 8 rows
+        const int grp = (warp - kEpiWarp0) >> 2;               // which rows of the 8
         const uint32_t lane_base = uint32_t(sp * 32) << 16;
         const float ninf = __int_as_float(0xff800000u);
         const int32_t N = int32_t(p.N);
         uint32_t ui = 0, g = 0, qi = 0;
-        float2 wa[kHeads / 2], wb[kHeads / 2];
         bool ok = true;
         while (ok) {
             const uint32_t slot = ui % kUnitSlots;
@@ -525,114 +636,94 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t qs = qi % kQSlots;
             if (!wait_bar_warp(bar(kBarQFull + qs), (qi / kQSlots) & 1u, ctl)) break;
             ++qi;
-            {
-                const float4* wsrc = reinterpret_cast<const float4*>(
-                    smem + kOffW + qs * kWBytes + quarter * kRowsPerEpiWarp * kHeads * 4);
+            // w of this warp's rows stays in shared memory for the whole unit; every lane
+            // reads the same address (a broadcast), 4 heads per 16-byte load
+            const float4* wsm = reinterpret_cast<const float4*>(
+                smem + kOffW + qs * kWBytes + grp * kRowsPerEpiWarp * kHeads * 4);
+
+            // This warp's rows: clamped windows, output rows, and the key tiles that lie
+            // inside every row's window (stored without compare/select).
+            const int64_t m_first = int64_t(info.m0) + grp * kRowsPerEpiWarp;
+            int32_t lo[kRowsPerEpiWarp], hi[kRowsPerEpiWarp];
+            bool rok[kRowsPerEpiWarp];
+            int32_t tcl = 0, tch = INT32_MAX;
 #pragma unroll
-                for (int j = 0; j < kHeads / 4; ++j) {
-                    const float4 x = wsrc[j];
-                    const float4 y = wsrc[kHeads / 4 + j];
-                    wa[2 * j] = make_float2(x.x, x.y);
-                    wa[2 * j + 1] = make_float2(x.z, x.w);
-                    wb[2 * j] = make_float2(y.x, y.y);
-                    wb[2 * j + 1] = make_float2(y.z, y.w);
-                }
+            for (int r = 0; r < kRowsPerEpiWarp; ++r) {
+                const int64_t m = m_first + r;
+                rok[r] = m < p.M;
+                lo[r] = rok[r] ? int32_t(clamp64(p.ks[m], 0, p.N)) : 0;
+                hi[r] = rok[r] ? int32_t(clamp64(p.ke[m], 0, p.N)) : 0;
+                tcl = max(tcl, (lo[r] + kTileKeys - 1) / kTileKeys);
+                tch = min(tch, hi[r] / kTileKeys);
             }
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(bar(kBarQEmpty + qs));
+            if (!rok[kRowsPerEpiWarp - 1]) tch = 0;  // rows past M take the masked path
+            float* row0 = p.out + m_first * p.N;
 
-            // This warp's two rows: clamped windows, output rows, and the key tiles that lie
-            // inside both windows (stored without compare/select).
-            const int64_t ma = int64_t(info.m0) + quarter * kRowsPerEpiWarp;
-            const bool oka = ma < p.M, okb = ma + 1 < p.M;
-            const int32_t loa = oka ? int32_t(clamp64(p.ks[ma], 0, p.N)) : 0;
-            const int32_t hia = oka ? int32_t(clamp64(p.ke[ma], 0, p.N)) : 0;
-            const int32_t lob = okb ? int32_t(clamp64(p.ks[ma + 1], 0, p.N)) : 0;
-            const int32_t hib = okb ? int32_t(clamp64(p.ke[ma + 1], 0, p.N)) : 0;
-            int32_t tcl = 0, tch = oka ? INT32_MAX : 0;
-            if (oka) {
-                tcl = max(tcl, (loa + kTileKeys - 1) / kTileKeys);
-                tch = min(tch, hia / kTileKeys);
-            }
-            if (okb) {
-                tcl = max(tcl, (lob + kTileKeys - 1) / kTileKeys);
-                tch = min(tch, hib / kTileKeys);
-            } else {
-                tch = 0;  // a missing second row takes the masked path
-            }
-            float* rowa = p.out + ma * p.N;
-            float* rowb = rowa + p.N;
-
+            // Per-tile state kept as toggles: accumulator buffer ab = g & 1 selects the
+            // barrier and TMEM column half, the barrier parity flips every second tile.
+            const uint32_t full0 = bar(kBarAccFull), empty0 = bar(kBarAccEmpty);
+            const uint32_t tm0 = tmem_base + lane_base + uint32_t(grp * kRowsPerEpiWarp * kHeads);
+            uint32_t ab = g & 1u, ph = (g >> 1) & 1u;
             int32_t n = info.t0 * kTileKeys + sp * 32 + lane;
-            float kv_next = n < N ? __ldg(p.kv_scale + n) : 0.f;
-            for (int32_t t = info.t0; t < info.t1; ++t, n += kTileKeys) {
+            const float* kvp = p.kv_scale + n;
+            float* op = row0 + n;  // row r of this warp at op + r * N
+            const int64_t rstride = p.N;
+            float kv_next = n < N ? __ldg(kvp) : 0.f;
+            for (int32_t t = info.t0; t < info.t1; ++t) {
                 const float kv = kv_next;
-                if (t + 1 < info.t1 && n + kTileKeys < N) kv_next = __ldg(p.kv_scale + n + kTileKeys);
-                const uint32_t ab = g & 1u;
-                if (!wait_bar_lane0(bar(kBarAccFull + ab), (g >> 1) & 1u, ctl)) {
+                kvp += kTileKeys;
+                if (t + 1 < info.t1 && n + kTileKeys < N) kv_next = __ldg(kvp);
+                if (!wait_bar_all(full0 + 8u * ab, ph, ctl)) {
                     ok = false;
                     break;
                 }
                 ptx::tc_fence_after();
-                const uint32_t taddr = tmem_base + lane_base + ab * kUmmaN +
-                                       uint32_t(quarter * kRowsPerEpiWarp * kHeads);
-                // sum_h relu(S[n, (m, h)]) * w[m, h] for the two rows, 16 heads per TMEM load
-                float va, vb;
+                const uint32_t taddr = tm0 + ab * kUmmaN;
+                // Copy all of this warp's accumulators out of TMEM and release the buffer at
+                // once, so the MMA can refill it while this warp does the arithmetic.
+                float v[kRowsPerEpiWarp];
                 {
-                    uint32_t s[16];
-                    float2 a[4];
+                    uint32_t s[kPairs][64];
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) a[c] = make_float2(0.f, 0.f);
-                    ptx::tmem_ld_32x32b_x16(taddr, s);
-                    ptx::tmem_wait_ld_regs16(s);
-                    relu_acc16(s, wa, a);
-                    ptx::tmem_ld_32x32b_x16(taddr + 16, s);
-                    ptx::tmem_wait_ld_regs16(s);
-                    relu_acc16(s, wa + 8, a);
-                    va = sum4(a);
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) a[c] = make_float2(0.f, 0.f);
-                    ptx::tmem_ld_32x32b_x16(taddr + kHeads, s);
-                    ptx::tmem_wait_ld_regs16(s);
-                    relu_acc16(s, wb, a);
-                    ptx::tmem_ld_32x32b_x16(taddr + kHeads + 16, s);
-                    ptx::tmem_wait_ld_regs16(s);
-                    // this warp's accumulator reads are done: release the buffer
+                    for (int pp = 0; pp < kPairs; ++pp)
+                        ptx::tmem_ld_32x32b_x64_sync(taddr + uint32_t(pp * 2 * kHeads), s[pp]);
                     ptx::tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) ptx::mbar_arrive(bar(kBarAccEmpty + ab));
-                    relu_acc16(s, wb + 8, a);
-                    vb = sum4(a);
+                    ptx::mbar_arrive(empty0 + 8u * ab);  // all 32 lanes arrive
+#pragma unroll
+                    for (int pp = 0; pp < kPairs; ++pp)
+                        relu_dot_2rows(s[pp], wsm + pp * 2 * (kHeads / 4), v[2 * pp], v[2 * pp + 1]);
                 }
-                va *= kv;
-                vb *= kv;
                 if (t >= tcl && t < tch) {
-                    // clean tile: inside both windows, so n < N and both rows exist
-                    __stcs(rowa + n, va);
-                    __stcs(rowb + n, vb);
+                    // clean tile: inside every row's window, so n < N and all rows exist
+#pragma unroll
+                    for (int r = 0; r < kRowsPerEpiWarp; ++r) __stcs(op + r * rstride, v[r] * kv);
                 } else if (n < N) {
-                    if (oka) {
-                        if (n >= loa && n < hia)
-                            __stcs(rowa + n, va);
+#pragma unroll
+                    for (int r = 0; r < kRowsPerEpiWarp; ++r) {
+                        if (!rok[r]) continue;
+                        if (n >= lo[r] && n < hi[r])
+                            __stcs(op + r * rstride, v[r] * kv);
                         else if (p.clean)
-                            __stcs(rowa + n, ninf);
-                    }
-                    if (okb) {
-                        if (n >= lob && n < hib)
-                            __stcs(rowb + n, vb);
-                        else if (p.clean)
-                            __stcs(rowb + n, ninf);
+                            __stcs(op + r * rstride, ninf);
                     }
                 }
+                n += kTileKeys;
+                op += kTileKeys;
+                ph ^= ab;
+                ab ^= 1u;
                 ++g;
             }
+            if (!ok) break;
+            // this warp is done with the unit's w
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(bar(kBarQEmpty + qs));
         }
     }
 
     // ---------------------------------------------------------------- teardown
     ptx::tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == kMmaWarp0) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem_base, kTmemCols);
     }
