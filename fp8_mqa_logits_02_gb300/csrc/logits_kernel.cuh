@@ -161,6 +161,11 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr)
     return d;
 }
 
+template <bool B>
+struct BoolTag {
+    static constexpr bool value = B;
+};
+
 struct Ctl {
     volatile int32_t* abort;
     int32_t* status;
@@ -665,18 +670,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t tm0 = tmem_base + lane_base + uint32_t(grp * kRowsPerEpiWarp * kHeads);
             uint32_t ab = g & 1u, ph = (g >> 1) & 1u;
             int32_t n = info.t0 * kTileKeys + sp * 32 + lane;
-            const float* kvp = p.kv_scale + n;
             float* op = row0 + n;  // row r of this warp at op + r * N
             const int64_t rstride = p.N;
-            float kv_next = n < N ? __ldg(kvp) : 0.f;
-            for (int32_t t = info.t0; t < info.t1; ++t) {
+            // kv_scale one tile ahead; past the end the index is clamped (the value is unused)
+            float kv_next = __ldg(p.kv_scale + min(n, N - 1));
+
+            // one tile; kClean: the tile lies inside every row's window (no compare/select)
+            auto step = [&](auto clean_tag) -> bool {
+                constexpr bool kClean = decltype(clean_tag)::value;
                 const float kv = kv_next;
-                kvp += kTileKeys;
-                if (t + 1 < info.t1 && n + kTileKeys < N) kv_next = __ldg(kvp);
-                if (!wait_bar_all(full0 + 8u * ab, ph, ctl)) {
-                    ok = false;
-                    break;
-                }
+                kv_next = __ldg(p.kv_scale + min(n + kTileKeys, N - 1));
+                if (!wait_bar_all(full0 + 8u * ab, ph, ctl)) return false;
                 ptx::tc_fence_after();
                 const uint32_t taddr = tm0 + ab * kUmmaN;
                 // Copy all of this warp's accumulators out of TMEM and release the buffer at
@@ -693,8 +697,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int pp = 0; pp < kPairs; ++pp)
                         relu_dot_2rows(s[pp], wsm + pp * 2 * (kHeads / 4), v[2 * pp], v[2 * pp + 1]);
                 }
-                if (t >= tcl && t < tch) {
-                    // clean tile: inside every row's window, so n < N and all rows exist
+                if (kClean) {
+                    // inside every row's window, so n < N and all rows exist
 #pragma unroll
                     for (int r = 0; r < kRowsPerEpiWarp; ++r) __stcs(op + r * rstride, v[r] * kv);
                 } else if (n < N) {
@@ -712,7 +716,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ph ^= ab;
                 ab ^= 1u;
                 ++g;
-            }
+                return true;
+            };
+            // masked head, clean middle, masked tail
+            const int32_t cs = max(info.t0, min(tcl, info.t1));
+            const int32_t ce = max(cs, min(tch, info.t1));
+            int32_t t = info.t0;
+            for (; ok && t < cs; ++t) ok = step(BoolTag<false>{});
+            for (; ok && t < ce; ++t) ok = step(BoolTag<true>{});
+            for (; ok && t < info.t1; ++t) ok = step(BoolTag<false>{});
             if (!ok) break;
             // this warp is done with the unit's w
             __syncwarp();
