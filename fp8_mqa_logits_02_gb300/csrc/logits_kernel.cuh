@@ -20,7 +20,8 @@
 //   warp 2      -inf writer (clean_logits = 1): fills every out-of-window span outside the
 //               computed tile range, on its own light-first unit order so the writes
 //               overlap the compute-heavy units (page: "With clean_logits the kernel writes
-//               -inf itself").
+//               -inf itself").  The spans go out as bulk copies from a shared-memory -inf
+//               buffer, so the TMA engine, not the issue slots the epilogue needs, does them.
 //   warps 4-19  epilogue, four warps per SM sub-partition, two query rows per warp:
 //               thread = one key (TMEM lane), so one tcgen05.ld gives it the 32 heads of
 //               one query row; relu, times w, head sum in registers (no cross-lane
@@ -47,7 +48,11 @@ namespace fp8mqa {
 
 constexpr int kHeads = 32;
 constexpr int kDim = 128;
-constexpr int kRows = 8;                  // query rows per unit
+// Query rows per unit (a multiple of 2, at most 8): kRows x 32 heads is the MMA N.
+#ifndef FP8MQA_ROWS
+#define FP8MQA_ROWS 8
+#endif
+constexpr int kRows = FP8MQA_ROWS;
 constexpr int kTileKeys = 128;            // keys per tile (MMA M)
 constexpr int kUmmaN = kRows * kHeads;    // 256 (MMA N)
 constexpr int kUmmaK = 32;                // FP8 K per tcgen05.mma
@@ -55,7 +60,8 @@ constexpr int kStages = 6;                // K ring depth
 constexpr int kQSlots = 3;
 constexpr int kUnitSlots = 4;
 constexpr int kAccBufs = 2;
-constexpr uint32_t kTmemCols = kAccBufs * kUmmaN;  // 512
+constexpr uint32_t kAccStride = 256;      // TMEM columns between accumulator buffers
+constexpr uint32_t kTmemCols = kAccBufs * kAccStride;  // 512 (a power of two)
 // Query rows each epilogue warp reduces per tile (2 or 4): more rows per warp amortise the
 // per-tile synchronisation over more arithmetic, fewer rows give more warps per SM.
 #ifndef FP8MQA_ROWS_PER_WARP
@@ -72,12 +78,14 @@ constexpr int kFillWarp = 2;
 constexpr uint32_t kQBytes = kRows * kHeads * kDim;   // 32768
 constexpr uint32_t kWBytes = kRows * kHeads * 4;      // 1024
 constexpr uint32_t kKBytes = kTileKeys * kDim;        // 16384
+constexpr uint32_t kFillBytes = 16384;                // -inf source for bulk stores
 
 // Shared-memory layout, offsets from a 1024-byte aligned base.
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffK = kOffQ + kQSlots * kQBytes;
 constexpr uint32_t kOffW = kOffK + kStages * kKBytes;
-constexpr uint32_t kOffBar = kOffW + kQSlots * kWBytes;
+constexpr uint32_t kOffFill = kOffW + kQSlots * kWBytes;
+constexpr uint32_t kOffBar = kOffFill + kFillBytes;
 
 constexpr int kBarKFull = 0;
 constexpr int kBarKEmpty = kBarKFull + kStages;
@@ -103,6 +111,9 @@ constexpr uint32_t kSmemUsed = kOffMisc + 16;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // slack for aligning the base
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 static_assert(kRowsPerEpiWarp == 2 || kRowsPerEpiWarp == 4, "two or four rows per warp");
+static_assert(kRows % kRowsPerEpiWarp == 0 && kRows <= 8 && kUmmaN <= int(kAccStride),
+              "rows per unit");
+static_assert(kQBytes % 1024 == 0 && kWBytes % 128 == 0, "shared-memory alignment");
 
 // Per-role register budgets (setmaxnreg): the control warpgroup gives registers to the
 // epilogue warpgroups; the total must stay within the launch allocation (threads x the
@@ -289,23 +300,27 @@ __device__ __forceinline__ Geometry unit_geometry(const Params& p, int32_t b, in
     return g;
 }
 
-// Warp-cooperative -inf fill of row[a, e) with streaming 16-byte stores.
-__device__ __forceinline__ void fill_neg_inf(float* row, int64_t a, int64_t e)
+// Warp-cooperative -inf fill of row[a, e): the 16-byte aligned middle goes out as bulk
+// copies (TMA engine) of up to kFillBytes from the shared-memory -inf buffer at `src`, issued
+// by lane 0; the ragged ends (under 4 floats each) are plain stores.
+__device__ __forceinline__ void fill_neg_inf(float* row, int64_t a, int64_t e, uint32_t src)
 {
     if (a >= e) return;
     const int lane = threadIdx.x & 31;
     const float ninf = __int_as_float(0xff800000u);
     const uintptr_t addr = reinterpret_cast<uintptr_t>(row + a);
-    int64_t head = int64_t(((16u - (addr & 15u)) & 15u) >> 2);
-    if (head > e - a) head = e - a;
-    if (lane < head) __stcs(row + a + lane, ninf);
-    a += head;
-    const int64_t nvec = (e - a) >> 2;
-    float4* v = reinterpret_cast<float4*>(row + a);
-    const float4 n4 = make_float4(ninf, ninf, ninf, ninf);
-    for (int64_t i = lane; i < nvec; i += 32) __stcs(v + i, n4);
-    a += nvec * 4;
-    if (lane < e - a) __stcs(row + a + lane, ninf);
+    int64_t a4 = a + int64_t(((16u - (addr & 15u)) & 15u) >> 2);
+    if (a4 > e) a4 = e;
+    const int64_t e4 = a4 + ((e - a4) & ~int64_t(3));
+    if (lane < a4 - a) __stcs(row + a + lane, ninf);
+    if (lane < e - e4) __stcs(row + e4 + lane, ninf);
+    if (lane == 0) {
+        constexpr int64_t kChunk = kFillBytes / 4;
+        for (int64_t x = a4; x < e4; x += kChunk) {
+            const int64_t c = e4 - x < kChunk ? e4 - x : kChunk;
+            ptx::bulk_store(row + x, src, uint32_t(c) * 4u);
+        }
+    }
 }
 
 __device__ __forceinline__ float2 relu2(uint32_t a, uint32_t b)
@@ -568,7 +583,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     ptx::tc_fence_after();
                     const uint64_t adesc = sw128_desc(sbase + kOffK + st * kKBytes);
-                    const uint32_t d = tmem_base + ab * kUmmaN;
+                    const uint32_t d = tmem_base + ab * kAccStride;
 #pragma unroll
                     for (int k = 0; k < kDim / kUmmaK; ++k) {
                         // advance 32 bytes along K inside the swizzle atom
@@ -588,8 +603,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
     } else if (warp < kEpiWarp0) {
-        // ------------------------------------------------------------ -inf writers
+        // ------------------------------------------------------------ -inf writer
         if (p.clean) {
+            const uint32_t src = sbase + kOffFill;
+            {
+                float4* f = reinterpret_cast<float4*>(smem + kOffFill);
+                const float ninf = __int_as_float(0xff800000u);
+                for (int i = lane; i < int(kFillBytes / 16); i += 32)
+                    f[i] = make_float4(ninf, ninf, ninf, ninf);
+                ptx::fence_proxy_async_smem();  // visible to the bulk copies
+                __syncwarp();
+            }
             while (true) {
                 uint32_t u = 0;
                 int stop = 0;
@@ -612,10 +636,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int64_t m = int64_t(geo.m0) + r;
                     if (m >= p.M) break;
                     float* row = p.out + m * p.N;
-                    fill_neg_inf(row, col_lo, left_end);
-                    fill_neg_inf(row, right_beg, col_hi);
+                    fill_neg_inf(row, col_lo, left_end, src);
+                    fill_neg_inf(row, right_beg, col_hi, src);
                 }
+                if (lane == 0) {
+                    // keep at most a few units' bulk copies queued
+                    ptx::bulk_commit();
+                    ptx::bulk_wait_read<4>();
+                }
+                __syncwarp();
             }
+            // every bulk copy has landed before the CTA (and its shared memory) goes away
+            if (lane == 0) ptx::bulk_wait_all();
+            __syncwarp();
         }
     } else {
         // ------------------------------------------------------------ epilogue
@@ -682,7 +715,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 kv_next = __ldg(p.kv_scale + min(n + kTileKeys, N - 1));
                 if (!wait_bar_all(full0 + 8u * ab, ph, ctl)) return false;
                 ptx::tc_fence_after();
-                const uint32_t taddr = tm0 + ab * kUmmaN;
+                const uint32_t taddr = tm0 + ab * kAccStride;
                 // Copy all of this warp's accumulators out of TMEM and release the buffer at
                 // once, so the MMA can refill it while this warp does the arithmetic.
                 float v[kRowsPerEpiWarp];
