@@ -347,7 +347,7 @@ def run_gpu(args):
 
 
 # Revision tag of the kernel the committed ncu traffic figure was taken on.
-KERNEL_REV = "v1"
+KERNEL_REV = "v2"
 
 
 def main(argv=None):
