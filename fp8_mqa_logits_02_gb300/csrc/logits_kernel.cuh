@@ -59,6 +59,7 @@ constexpr int kUmmaK = 32;                // FP8 K per tcgen05.mma
 constexpr int kStages = 6;                // K ring depth
 constexpr int kQSlots = 3;
 constexpr int kUnitSlots = 4;
+constexpr int kClaimAhead = 4;           // K tiles of a unit left to issue when the next is claimed
 constexpr int kAccBufs = 2;
 constexpr uint32_t kAccStride = 256;      // TMEM columns between accumulator buffers
 constexpr uint32_t kTmemCols = kAccBufs * kAccStride;  // 512 (a power of two)
@@ -102,6 +103,7 @@ struct UnitInfo {
     int32_t m0;      // first query row
     int32_t t0, t1;  // key tiles [t0, t1) computed by MMA + epilogue
     int32_t flags;   // kUnitTerminate
+    int32_t lo[kRows], hi[kRows];  // each row's window clamped to [0, N); rows past M: empty
 };
 constexpr int32_t kUnitTerminate = 1;
 
@@ -262,6 +264,8 @@ __device__ __forceinline__ int64_t clamp64(int64_t v, int64_t lo, int64_t hi)
 // Key tiles [t0, t1) are those of chunk c that meet the union of the block's windows.
 struct Geometry {
     int32_t m0, t0, t1, ct0, ct1;
+    int32_t ut0, ut1;  // key tiles meeting the union of the block's windows (empty: ut0 >= ut1)
+    int32_t lo, hi;  // lane r < kRows: row m0 + r's window clamped to [0, N) (empty past M)
 };
 
 __device__ __forceinline__ Geometry unit_geometry(const Params& p, int32_t b, int32_t c)
@@ -270,10 +274,14 @@ __device__ __forceinline__ Geometry unit_geometry(const Params& p, int32_t b, in
     Geometry g;
     g.m0 = b * kRows;
     int64_t lo = INT64_MAX, hi = INT64_MIN;
+    g.lo = 0;
+    g.hi = 0;
     if (lane < kRows && g.m0 + lane < p.M) {
         const int64_t m = g.m0 + lane;
         const int64_t s = clamp64(p.ks[m], 0, p.N);
         const int64_t e = clamp64(p.ke[m], 0, p.N);
+        g.lo = int32_t(s);
+        g.hi = int32_t(e);
         if (s < e) {
             lo = s;
             hi = e;
@@ -290,12 +298,16 @@ __device__ __forceinline__ Geometry unit_geometry(const Params& p, int32_t b, in
     g.ct1 = min(g.ct0 + p.tiles_per_chunk, p.num_tiles);
     g.t0 = g.ct0;
     g.t1 = g.ct0;
-    if (lo < hi && g.ct0 < g.ct1) {
-        const int32_t a = int32_t(lo / kTileKeys);
-        const int32_t e = int32_t((hi + kTileKeys - 1) / kTileKeys);
-        g.t0 = max(g.ct0, a);
-        g.t1 = min(g.ct1, e);
-        if (g.t1 < g.t0) g.t1 = g.t0;
+    g.ut0 = 0;
+    g.ut1 = 0;
+    if (lo < hi) {
+        g.ut0 = int32_t(lo / kTileKeys);
+        g.ut1 = int32_t((hi + kTileKeys - 1) / kTileKeys);
+        if (g.ct0 < g.ct1) {
+            g.t0 = max(g.ct0, g.ut0);
+            g.t1 = min(g.ct1, g.ut1);
+            if (g.t1 < g.t0) g.t1 = g.t0;
+        }
     }
     return g;
 }
@@ -482,60 +494,118 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t pol_k = ptx::policy_evict_last();
         const uint64_t pol_q = ptx::policy_evict_first();
         uint32_t ui = 0, g = 0, qi = 0;
-        while (true) {
-            uint32_t u = 0;
-            int stop = 0;
-            if (lane == 0) {
-                u = atomicAdd(&p.sched->next_unit, 1u);
-                stop = (u >= uint32_t(p.num_units) || *abort_flag) ? 1 : 0;
-            }
-            u = __shfl_sync(0xffffffffu, u, 0);
-            stop = __shfl_sync(0xffffffffu, stop, 0);
-            UnitInfo info{0, 0, 0, 0};
-            if (stop) {
-                info.flags = kUnitTerminate;
-            } else {
+        // Claim the next unit with key tiles (empty units are skipped here, never published);
+        // every lane returns the same unit, lane r < kRows also its row's window.
+        auto claim = [&]() -> Geometry {
+            while (true) {
+                uint32_t u = 0;
+                int stop = 0;
+                if (lane == 0) {
+                    u = atomicAdd(&p.sched->next_unit, 1u);
+                    stop = (u >= uint32_t(p.num_units) || *abort_flag) ? 1 : 0;
+                }
+                u = __shfl_sync(0xffffffffu, u, 0);
+                if (__shfl_sync(0xffffffffu, stop, 0)) {
+                    Geometry none{};
+                    none.m0 = -1;
+                    return none;
+                }
                 const int32_t b = p.num_blocks - 1 - int32_t(u / uint32_t(p.split));
                 const int32_t c = int32_t(u % uint32_t(p.split));
                 const Geometry geo = unit_geometry(p, b, c);
-                info.m0 = geo.m0;
-                info.t0 = geo.t0;
-                info.t1 = geo.t1;
-            }
-            int ok = 1;
-            if (lane == 0) {
-                const uint32_t slot = ui % kUnitSlots;
-                ok = wait_bar(bar(kBarUnitEmpty + slot), ((ui / kUnitSlots) & 1u) ^ 1u, ctl);
-                if (ok) {
-                    units[slot] = info;
-                    ptx::mbar_arrive(bar(kBarUnitFull + slot));
+                // The block's chunks that meet its windows are [c_lo, c_hi]; move the shared
+                // counter past the empty ones this claim has revealed, so no CTA spends a
+                // claim on them (a hint: a unit that is claimed anyway is found empty).
+                if (lane == 0) {
+                    const uint32_t base = u - uint32_t(c);
+                    if (geo.ut0 >= geo.ut1) {
+                        atomicMax(&p.sched->next_unit, base + uint32_t(p.split));
+                    } else {
+                        const int32_t c_lo = geo.ut0 / p.tiles_per_chunk;
+                        const int32_t c_hi = (geo.ut1 - 1) / p.tiles_per_chunk;
+                        if (c < c_lo)
+                            atomicMax(&p.sched->next_unit, base + uint32_t(c_lo));
+                        else if (c >= c_hi)
+                            atomicMax(&p.sched->next_unit, base + uint32_t(p.split));
+                    }
                 }
-                if (ok && !(info.flags & kUnitTerminate) && info.t1 > info.t0) {
+                if (geo.t1 > geo.t0) return geo;
+            }
+        };
+        // Publish a unit to the consumers (m0 < 0: the terminate marker) and start its Q + w
+        // load.  Returns false when the CTA is aborting.
+        auto publish = [&](const Geometry& geo) -> bool {
+            const uint32_t slot = ui % kUnitSlots;
+            int ok = 1;
+            if (lane == 0) ok = wait_bar(bar(kBarUnitEmpty + slot), ((ui / kUnitSlots) & 1u) ^ 1u, ctl);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) return false;
+            UnitInfo& dst = units[slot];
+            if (lane < kRows) {
+                dst.lo[lane] = geo.lo;
+                dst.hi[lane] = geo.hi;
+            }
+            if (lane == 0) {
+                dst.m0 = geo.m0;
+                dst.t0 = geo.t0;
+                dst.t1 = geo.t1;
+                dst.flags = geo.m0 < 0 ? kUnitTerminate : 0;
+            }
+            __syncwarp();
+            if (lane == 0) {
+                ptx::mbar_arrive(bar(kBarUnitFull + slot));
+                if (geo.m0 >= 0) {
                     const uint32_t qs = qi % kQSlots;
                     ok = wait_bar(bar(kBarQEmpty + qs), ((qi / kQSlots) & 1u) ^ 1u, ctl);
                     if (ok) {
                         const uint32_t fb = bar(kBarQFull + qs);
                         ptx::mbar_arrive_expect_tx(fb, kQBytes + kWBytes);
                         ptx::tma_load_2d_hint(sbase + kOffQ + qs * kQBytes, &tm_q, fb, 0,
-                                              info.m0 * kHeads, pol_q);
-                        ptx::tma_load_2d(sbase + kOffW + qs * kWBytes, &tm_w, fb, 0, info.m0);
+                                              geo.m0 * kHeads, pol_q);
+                        ptx::tma_load_2d(sbase + kOffW + qs * kWBytes, &tm_w, fb, 0, geo.m0);
                         ++qi;
-                    }
-                    for (int32_t t = info.t0; ok && t < info.t1; ++t) {
-                        const uint32_t st = g % kStages;
-                        ok = wait_bar(bar(kBarKEmpty + st), ((g / kStages) & 1u) ^ 1u, ctl);
-                        if (!ok) break;
-                        const uint32_t fb = bar(kBarKFull + st);
-                        ptx::mbar_arrive_expect_tx(fb, kKBytes);
-                        ptx::tma_load_2d_hint(sbase + kOffK + st * kKBytes, &tm_k, fb, 0,
-                                              t * kTileKeys, pol_k);
-                        ++g;
                     }
                 }
             }
             ++ui;
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok || (info.flags & kUnitTerminate)) break;
+            return __shfl_sync(0xffffffffu, ok, 0) != 0;
+        };
+        // One unit of lookahead: the next unit is claimed, published and its Q requested
+        // while the current unit's last kClaimAhead K tiles are still to be issued (plus the
+        // kStages in the ring), so the claim's global round trips and the Q load hide behind
+        // them.  Claiming earlier would hold units back from CTAs that finish first.
+        Geometry cur = claim();
+        bool ok = publish(cur);
+        while (ok && cur.m0 >= 0) {
+            Geometry nxt{};
+            bool have_nxt = false;
+            const int32_t claim_at = max(cur.t0, cur.t1 - kClaimAhead);
+            for (int32_t t = cur.t0; ok && t < cur.t1; ++t) {
+                if (t == claim_at) {
+                    nxt = claim();
+                    ok = publish(nxt);
+                    have_nxt = true;
+                    if (!ok) break;
+                }
+                int issued = 1;
+                if (lane == 0) {
+                    const uint32_t st = g % kStages;
+                    issued = wait_bar(bar(kBarKEmpty + st), ((g / kStages) & 1u) ^ 1u, ctl) ? 1 : 0;
+                    if (issued) {
+                        const uint32_t fb = bar(kBarKFull + st);
+                        ptx::mbar_arrive_expect_tx(fb, kKBytes);
+                        ptx::tma_load_2d_hint(sbase + kOffK + st * kKBytes, &tm_k, fb, 0,
+                                              t * kTileKeys, pol_k);
+                    }
+                }
+                ok = __shfl_sync(0xffffffffu, issued, 0) != 0;
+                if (ok) ++g;
+            }
+            if (ok && !have_nxt) {
+                nxt = claim();
+                ok = publish(nxt);
+            }
+            cur = nxt;
         }
         if (lane == 0) {
             // Wait for any TMA load still in flight before the CTA can exit: only the last
@@ -557,16 +627,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             while (ok) {
                 const uint32_t slot = ui % kUnitSlots;
                 if (!wait_bar(bar(kBarUnitFull + slot), (ui / kUnitSlots) & 1u, ctl)) break;
-                const UnitInfo info = units[slot];
+                const int32_t flags = units[slot].flags;
+                const int32_t ut0 = units[slot].t0, ut1 = units[slot].t1;
                 ptx::mbar_arrive(bar(kBarUnitEmpty + slot));
                 ++ui;
-                if (info.flags & kUnitTerminate) break;
-                if (info.t1 <= info.t0) continue;
+                if (flags & kUnitTerminate) break;
                 const uint32_t qs = qi % kQSlots;
                 if (!wait_bar(bar(kBarQFull + qs), (qi / kQSlots) & 1u, ctl)) break;
                 ++qi;
                 const uint64_t bdesc = sw128_desc(sbase + kOffQ + qs * kQBytes);
-                for (int32_t t = info.t0; t < info.t1; ++t) {
+                for (int32_t t = ut0; t < ut1; ++t) {
                     const uint32_t st = g % kStages;
                     const uint32_t ab = g & 1u;
                     if (ab != par) {  // the other issuer's tile
@@ -664,12 +734,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         while (ok) {
             const uint32_t slot = ui % kUnitSlots;
             if (!wait_bar_warp(bar(kBarUnitFull + slot), (ui / kUnitSlots) & 1u, ctl)) break;
-            const UnitInfo info = units[slot];
+            // the unit and this warp's rows' windows, copied out before the slot is released
+            const UnitInfo& src = units[slot];
+            const int32_t flags = src.flags, m0 = src.m0, t0 = src.t0, t1 = src.t1;
+            int32_t lo[kRowsPerEpiWarp], hi[kRowsPerEpiWarp];
+#pragma unroll
+            for (int r = 0; r < kRowsPerEpiWarp; ++r) {
+                lo[r] = src.lo[grp * kRowsPerEpiWarp + r];
+                hi[r] = src.hi[grp * kRowsPerEpiWarp + r];
+            }
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(bar(kBarUnitEmpty + slot));
             ++ui;
-            if (info.flags & kUnitTerminate) break;
-            if (info.t1 <= info.t0) continue;
+            if (flags & kUnitTerminate) break;
 
             const uint32_t qs = qi % kQSlots;
             if (!wait_bar_warp(bar(kBarQFull + qs), (qi / kQSlots) & 1u, ctl)) break;
@@ -679,18 +756,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float4* wsm = reinterpret_cast<const float4*>(
                 smem + kOffW + qs * kWBytes + grp * kRowsPerEpiWarp * kHeads * 4);
 
-            // This warp's rows: clamped windows, output rows, and the key tiles that lie
-            // inside every row's window (stored without compare/select).
-            const int64_t m_first = int64_t(info.m0) + grp * kRowsPerEpiWarp;
-            int32_t lo[kRowsPerEpiWarp], hi[kRowsPerEpiWarp];
+            // This warp's rows: output rows, and the key tiles that lie inside every row's
+            // window (stored without compare/select).
+            const int64_t m_first = int64_t(m0) + grp * kRowsPerEpiWarp;
             bool rok[kRowsPerEpiWarp];
             int32_t tcl = 0, tch = INT32_MAX;
 #pragma unroll
             for (int r = 0; r < kRowsPerEpiWarp; ++r) {
-                const int64_t m = m_first + r;
-                rok[r] = m < p.M;
-                lo[r] = rok[r] ? int32_t(clamp64(p.ks[m], 0, p.N)) : 0;
-                hi[r] = rok[r] ? int32_t(clamp64(p.ke[m], 0, p.N)) : 0;
+                rok[r] = m_first + r < p.M;
                 tcl = max(tcl, (lo[r] + kTileKeys - 1) / kTileKeys);
                 tch = min(tch, hi[r] / kTileKeys);
             }
@@ -702,7 +775,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t full0 = bar(kBarAccFull), empty0 = bar(kBarAccEmpty);
             const uint32_t tm0 = tmem_base + lane_base + uint32_t(grp * kRowsPerEpiWarp * kHeads);
             uint32_t ab = g & 1u, ph = (g >> 1) & 1u;
-            int32_t n = info.t0 * kTileKeys + sp * 32 + lane;
+            int32_t n = t0 * kTileKeys + sp * 32 + lane;
             float* op = row0 + n;  // row r of this warp at op + r * N
             const int64_t rstride = p.N;
             // kv_scale one tile ahead; past the end the index is clamped (the value is unused)
@@ -752,12 +825,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 return true;
             };
             // masked head, clean middle, masked tail
-            const int32_t cs = max(info.t0, min(tcl, info.t1));
-            const int32_t ce = max(cs, min(tch, info.t1));
-            int32_t t = info.t0;
+            const int32_t cs = max(t0, min(tcl, t1));
+            const int32_t ce = max(cs, min(tch, t1));
+            int32_t t = t0;
             for (; ok && t < cs; ++t) ok = step(BoolTag<false>{});
             for (; ok && t < ce; ++t) ok = step(BoolTag<true>{});
-            for (; ok && t < info.t1; ++t) ok = step(BoolTag<false>{});
+            for (; ok && t < t1; ++t) ok = step(BoolTag<false>{});
             if (!ok) break;
             // this warp is done with the unit's w
             __syncwarp();

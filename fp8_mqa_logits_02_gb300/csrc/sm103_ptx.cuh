@@ -64,6 +64,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
+// Non-blocking test of whether the phase with the given parity has completed.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Like mbar_try_wait, but the thread may sleep up to `suspend_ns` nanoseconds waiting for
 // the phase to complete (it wakes as soon as it does) instead of returning at once.
 __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity,

@@ -60,10 +60,11 @@ def test_is_supported_truth_table(lib):
 
 
 def test_default_split(lib):
-    # about 8 units per SM when row blocks are few, chunks of at least 8 key tiles
+    # about 8 units per SM (16 when there are under two row blocks per SM), chunks of at
+    # least 8 key tiles
     assert fm.default_split(8192, 8192, 152) == 2
     assert fm.default_split(4096, 32768, 152) == 3
-    assert fm.default_split(1024, 131072, 152) == 10
+    assert fm.default_split(1024, 131072, 152) == 19
     assert fm.default_split(64, 256, 152) == 1
     assert fm.default_split(1, 1, 152) == 1
     for M in (1, 7, 100, 5000):
