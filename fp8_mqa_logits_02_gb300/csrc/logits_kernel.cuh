@@ -179,6 +179,11 @@ struct BoolTag {
     static constexpr bool value = B;
 };
 
+template <int V>
+struct IntTag {
+    static constexpr int value = V;
+};
+
 struct Ctl {
     volatile int32_t* abort;
     int32_t* status;
@@ -770,22 +775,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!rok[kRowsPerEpiWarp - 1]) tch = 0;  // rows past M take the masked path
             float* row0 = p.out + m_first * p.N;
 
-            // Per-tile state kept as toggles: accumulator buffer ab = g & 1 selects the
-            // barrier and TMEM column half, the barrier parity flips every second tile.
+            // Per-tile state: accumulator buffer ab = g & 1 selects the barrier and the TMEM
+            // column half, the barrier parity ph flips after every buffer-1 tile.
             const uint32_t full0 = bar(kBarAccFull), empty0 = bar(kBarAccEmpty);
             const uint32_t tm0 = tmem_base + lane_base + uint32_t(grp * kRowsPerEpiWarp * kHeads);
-            uint32_t ab = g & 1u, ph = (g >> 1) & 1u;
+            uint32_t ph = (g >> 1) & 1u;
             int32_t n = t0 * kTileKeys + sp * 32 + lane;
-            float* op = row0 + n;  // row r of this warp at op + r * N
-            const int64_t rstride = p.N;
+            float* op[kRowsPerEpiWarp];  // this lane's output element in each of the warp's rows
+#pragma unroll
+            for (int r = 0; r < kRowsPerEpiWarp; ++r) op[r] = row0 + r * p.N + n;
+            const float* const kvp = p.kv_scale;
+            const int32_t n_last = N - 1;
+            const bool clean_out = p.clean != 0;
             // kv_scale one tile ahead; past the end the index is clamped (the value is unused)
-            float kv_next = __ldg(p.kv_scale + min(n, N - 1));
+            float kv_next = __ldg(kvp + min(n, n_last));
 
-            // one tile; kClean: the tile lies inside every row's window (no compare/select)
-            auto step = [&](auto clean_tag) -> bool {
+            // One tile.  kClean: the tile lies inside every row's window (no compare/select).
+            // kAB: the accumulator buffer when known at compile time (the clean middle runs in
+            // buffer pairs), -1 when it comes from the tile count.
+            auto step = [&](auto clean_tag, auto ab_tag) -> bool {
                 constexpr bool kClean = decltype(clean_tag)::value;
+                constexpr int kAB = decltype(ab_tag)::value;
+                const uint32_t ab = kAB >= 0 ? uint32_t(kAB) : (g & 1u);
                 const float kv = kv_next;
-                kv_next = __ldg(p.kv_scale + min(n + kTileKeys, N - 1));
+                kv_next = __ldg(kvp + min(n + kTileKeys, n_last));
                 if (!wait_bar_all(full0 + 8u * ab, ph, ctl)) return false;
                 ptx::tc_fence_after();
                 const uint32_t taddr = tm0 + ab * kAccStride;
@@ -806,31 +819,42 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (kClean) {
                     // inside every row's window, so n < N and all rows exist
 #pragma unroll
-                    for (int r = 0; r < kRowsPerEpiWarp; ++r) __stcs(op + r * rstride, v[r] * kv);
+                    for (int r = 0; r < kRowsPerEpiWarp; ++r) __stcs(op[r], v[r] * kv);
                 } else if (n < N) {
 #pragma unroll
                     for (int r = 0; r < kRowsPerEpiWarp; ++r) {
                         if (!rok[r]) continue;
                         if (n >= lo[r] && n < hi[r])
-                            __stcs(op + r * rstride, v[r] * kv);
-                        else if (p.clean)
-                            __stcs(op + r * rstride, ninf);
+                            __stcs(op[r], v[r] * kv);
+                        else if (clean_out)
+                            __stcs(op[r], ninf);
                     }
                 }
                 n += kTileKeys;
-                op += kTileKeys;
+#pragma unroll
+                for (int r = 0; r < kRowsPerEpiWarp; ++r) op[r] += kTileKeys;
                 ph ^= ab;
-                ab ^= 1u;
                 ++g;
                 return true;
             };
-            // masked head, clean middle, masked tail
+            // masked head, clean middle (in buffer pairs), masked tail
             const int32_t cs = max(t0, min(tcl, t1));
             const int32_t ce = max(cs, min(tch, t1));
             int32_t t = t0;
-            for (; ok && t < cs; ++t) ok = step(BoolTag<false>{});
-            for (; ok && t < ce; ++t) ok = step(BoolTag<true>{});
-            for (; ok && t < t1; ++t) ok = step(BoolTag<false>{});
+            for (; ok && t < cs; ++t) ok = step(BoolTag<false>{}, IntTag<-1>{});
+            if (ok && t < ce && (g & 1u)) {
+                ok = step(BoolTag<true>{}, IntTag<-1>{});
+                ++t;
+            }
+            for (; ok && t + 1 < ce; t += 2) {
+                ok = step(BoolTag<true>{}, IntTag<0>{});
+                if (ok) ok = step(BoolTag<true>{}, IntTag<1>{});
+            }
+            if (ok && t < ce) {
+                ok = step(BoolTag<true>{}, IntTag<-1>{});
+                ++t;
+            }
+            for (; ok && t < t1; ++t) ok = step(BoolTag<false>{}, IntTag<-1>{});
             if (!ok) break;
             // this warp is done with the unit's w
             __syncwarp();
