@@ -347,7 +347,7 @@ def run_gpu(args):
 
 
 # Revision tag of the kernel the committed ncu traffic figure was taken on.
-KERNEL_REV = "v2"
+KERNEL_REV = "v3"
 
 
 def main(argv=None):
