@@ -173,6 +173,9 @@ def _sample_rows(M, nrand, seed):
     ("long_causal_1024x131072", True, 0),
     ("multi_req_4096x32768", True, 0),
     ("multi_req_4096x32768", True, 20),
+    ("kpool_causal_16384x32000", True, 0),
+    ("cp_4096x32768", True, 0),
+    ("cp_4096x32768", False, 3),
 ])
 def test_full_workloads_sampled(name, clean, split_n):
     wl = workloads.WORKLOADS[name]
@@ -198,3 +201,27 @@ def test_full_workloads_sampled(name, clean, split_n):
     gpu = out[torch.from_numpy(rows).cuda()].cpu().numpy()
     assert_parity(gpu, ref, window_mask(inp["ks"], inp["ke"], N, rows), clean,
                   what=f"{name} clean={clean} split={split_n}")
+
+
+def test_call_captured_in_a_cuda_graph():
+    # After the first call on the device (which sets up the library's scratch), a call can be
+    # captured on a stream and replayed; every replay recomputes the whole output.
+    inp = _inputs(200, 3000, "misaligned", seed=13)
+    dev = to_device(inp)
+    ref = run_oracle(inp, clean=True)
+    inside = window_mask(inp["ks"], inp["ke"], inp["N"])
+    out = poisoned(200, 3000)
+    fm.fp8_mqa_logits(dev["q"], dev["k"], dev["kv_scale"], dev["w"], dev["ks"], dev["ke"],
+                      out=out)
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        fm.fp8_mqa_logits(dev["q"], dev["k"], dev["kv_scale"], dev["w"], dev["ks"], dev["ke"],
+                          out=out, stream=s)
+    for _ in range(3):
+        out.copy_(poisoned(200, 3000))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert fm.check_error() == 0
+        assert_parity(out.cpu().numpy(), ref, inside, True, what="graph replay")

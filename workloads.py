@@ -8,12 +8,13 @@ Distributions (the same for every workload): Q and K are N(0,1) draws clipped to
 N(0,1)/sqrt(H*D) in fp32; kv_scale is U[0.5, 2] in fp32.  One CPU ``torch.Generator``
 seeded with the workload's seed draws Q, K, w and kv_scale in that order.
 
-Window families.  The five benchmark workloads follow the kernel-time table of
+Window families.  The benchmark workloads follow the kernel-time table of
 ROCm/aiter PR #7183 ("Kernel time on the GLM-5.3-Flash table shapes"): causal chunks
-whose query rows are the last M positions of an N-key context, and a multi-request
-chunk of four requests.  The test-only families ("cp", "misaligned", "empty",
-"past_end") are readings of the op-test window modes named in the same page's
-"Test plan"; the page does not define them, so each is spelled out below.
+whose query rows are the last M positions of an N-key context, a multi-request chunk of
+four requests, and the table's "16384 x 32000 (kpool 4)" row.  The other families
+("cp", "misaligned", "empty", "past_end") are readings of the op-test window modes named
+in the same page's "Test plan"; the page does not define them, so each is spelled out
+below.
 """
 from __future__ import annotations
 
@@ -39,7 +40,7 @@ class Workload:
     requests: int = 1  # multi_req only
 
 
-# The five benchmark/parity workloads (seed = position in this list).
+# The benchmark/parity workloads (seed = position in this list).
 WORKLOADS = {
     "tiny_causal_64x256": Workload("tiny_causal_64x256", 64, 256, "causal", 0),
     "causal_8192x8192": Workload("causal_8192x8192", 8192, 8192, "causal", 1),
@@ -47,6 +48,11 @@ WORKLOADS = {
     "long_causal_1024x131072": Workload("long_causal_1024x131072", 1024, 131072, "causal", 3),
     "multi_req_4096x32768": Workload("multi_req_4096x32768", 4096, 32768, "multi_req", 4,
                                      requests=4),
+    # The same table's "16384 x 32000 (kpool 4)" row, read as one causal chunk over a single
+    # contiguous K of 32000 keys (the page does not define "kpool"), and the chunk shape
+    # under the context-parallel window family of the page's op test.
+    "kpool_causal_16384x32000": Workload("kpool_causal_16384x32000", 16384, 32000, "causal", 5),
+    "cp_4096x32768": Workload("cp_4096x32768", 4096, 32768, "cp", 6),
 }
 
 WINDOW_FAMILIES = ("causal", "cp", "misaligned", "empty", "past_end", "multi_req")
