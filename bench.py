@@ -346,6 +346,55 @@ def run_gpu(args):
     return 0
 
 
+def run_topk(args):
+    """Time fp8_mqa_topk on the logits of a workload: one step is the top-k of every row."""
+    import torch
+
+    import fp8_mqa_logits_02_gb300 as fm
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    wl = workloads.WORKLOADS[args.workload]
+    inp = workloads.make(wl)
+    M, N = inp["M"], inp["N"]
+    t = {key: torch.from_numpy(inp[key]).to(dev) for key in ("q", "k", "kv_scale", "w", "ks", "ke")}
+    logits = fm.fp8_mqa_logits(t["q"].view(torch.float8_e4m3fn), t["k"].view(torch.float8_e4m3fn),
+                               t["kv_scale"], t["w"], t["ks"], t["ke"])
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(args.warmup):
+        flush.zero_()
+        fm.topk(logits, args.topk, stream=stream)
+    torch.cuda.synchronize(dev)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with ClockSampler(dev.index) as clocks:
+        for i in range(args.steps):
+            flush.zero_()
+            starts[i].record(stream)
+            fm.topk(logits, args.topk, stream=stream)
+            ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+    ms = statistics.mean(s.elapsed_time(e) for s, e in zip(starts, ends))
+    algo_bytes = M * N * 4 + M * args.topk * 8
+    peaks = load_peaks()
+    gbs = algo_bytes / (ms * 1e-3) / 1e9
+    print(json.dumps({
+        "metric": "per-row top-k over the logits, GB/s of algorithmic traffic",
+        "value": gbs, "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "us_per_call": ms * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": wl.name, "M": M, "N": N, "k": args.topk,
+                   "l2": f"flushed before every timed call ({FLUSH_BYTES >> 20} MiB write)"},
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": gbs / peaks["hbm_gbs"], "traffic": None,
+                     "peak_source": f"{peaks['source']} copy bandwidth",
+                     "kernel": "topk_kernel"},
+        "gpu_launches": args.steps, "clocks": clocks.summary(),
+    }), flush=True)
+    return 0
+
+
 # Revision tag of the kernel the committed ncu traffic figure was taken on.
 KERNEL_REV = "v3"
 
@@ -360,6 +409,8 @@ def main(argv=None):
     ap.add_argument("--split-n", type=int, default=0)
     ap.add_argument("--impl", default="native", choices=("native", "reference"))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--topk", type=int, default=0,
+                    help="time the per-row top-k (this k) over the workload's logits instead")
     ap.add_argument("--reference-rows", type=int, default=4096,
                     help="query rows of the workload the CPU-baseline sample computes")
     args = ap.parse_args(argv)
@@ -367,6 +418,8 @@ def main(argv=None):
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.topk:
+        return run_topk(args)
     return run_gpu(args)
 
 

@@ -49,7 +49,10 @@ SIGNATURES = {
     "fp8_mqa_logits_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "fp8_mqa_logits_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I32,
                                               _I32, _I32, _I32, _P]),
+    "fp8_mqa_topk": (ctypes.c_int, [_P, _I64, _I64, _I64, _I32, _P, _P, _P]),
 }
+
+TOPK_MAX_K = 2048
 
 
 class Fp8MqaError(RuntimeError):
@@ -157,6 +160,37 @@ def fp8_mqa_logits(q: torch.Tensor, k: torch.Tensor, kv_scale: torch.Tensor, w: 
     if rc != 0:
         raise Fp8MqaError(rc, "fp8_mqa_logits")
     return out
+
+
+def topk(logits: torch.Tensor, k: int, with_values: bool = True, stream=None):
+    """Per-row top-k of a float32 [M, N] CUDA tensor (rows may be strided, elements not).
+
+    Returns (indices int32 [M, k], values float32 [M, k] or None): the k largest finite
+    entries of each row, by value descending and equal values by index ascending; slots past
+    a row's finite entries hold -1 / -inf.  Asynchronous on ``stream``.
+    """
+    _check_strided_rows(logits, "logits")
+    if not 1 <= int(k) <= TOPK_MAX_K:
+        raise ValueError(f"k must be in [1, {TOPK_MAX_K}]")
+    M, N = logits.shape
+    dev = logits.device
+    idx = torch.empty((M, int(k)), dtype=torch.int32, device=dev)
+    val = torch.empty((M, int(k)), dtype=torch.float32, device=dev) if with_values else None
+    with torch.cuda.device(dev):
+        rc = lib().fp8_mqa_topk(logits.data_ptr(), M, N, logits.stride(0), int(k), idx.data_ptr(),
+                                val.data_ptr() if val is not None else None, _stream_ptr(stream))
+    if rc != 0:
+        raise Fp8MqaError(rc, "fp8_mqa_topk")
+    return idx, val
+
+
+def _check_strided_rows(t: torch.Tensor, name: str):
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor (the library has no CPU path)")
+    if t.dtype != torch.float32 or t.dim() != 2:
+        raise ValueError(f"{name} must be float32 [M, N]")
+    if t.shape[1] > 1 and t.stride(1) != 1:
+        raise ValueError(f"{name} rows must be contiguous")
 
 
 def check_error(stream=None) -> int:

@@ -13,6 +13,7 @@
 
 #include "../../include/fp8_mqa_logits.h"
 #include "logits_kernel.cuh"
+#include "topk_kernel.cuh"
 
 namespace fp8mqa {
 namespace {
@@ -429,6 +430,36 @@ int fp8_mqa_logits_noalloc(const uint8_t* q_fp8, const uint8_t* k_fp8, const flo
     if (rc != FP8MQA_OK || M == 0 || N == 0) return rc;
     return fp8mqa::launch_noalloc(q_fp8, k_fp8, kv_scale, w, ks, ke, out, M, N, clean_logits,
                                   split_n, static_cast<cudaStream_t>(stream));
+}
+
+int fp8_mqa_topk(const float* logits, int64_t M, int64_t N, int64_t ld, int32_t k,
+                 int32_t* indices, float* values, void* stream)
+{
+    if (M < 0 || N < 0 || ld < N || k < 1 || k > fp8mqa::kTopkMaxK) return FP8MQA_ERR_INVALID_ARG;
+    if (N > (int64_t(1) << 30)) return FP8MQA_ERR_UNSUPPORTED_SHAPE;
+    if (M == 0) return FP8MQA_OK;
+    if (!indices || (N > 0 && !logits)) return FP8MQA_ERR_INVALID_ARG;
+    if (!fp8mqa::aligned(logits, 4) || !fp8mqa::aligned(indices, 4) ||
+        (values && !fp8mqa::aligned(values, 4)))
+        return FP8MQA_ERR_MISALIGNED;
+    int err = FP8MQA_OK;
+    fp8mqa::DeviceState* st = fp8mqa::device_state(&err);
+    if (!st) return err;
+    fp8mqa::TopkParams p;
+    p.logits = logits;
+    p.M = M;
+    p.N = N;
+    p.ld = ld;
+    p.k = k;
+    p.indices = indices;
+    p.values = values;
+    // one CTA per SM, each walking rows: the rows in flight stay resident in L2 for the
+    // select's re-reads
+    const int64_t grid = M < st->sm_count ? M : st->sm_count;
+    fp8mqa::topk_kernel<<<dim3(uint32_t(grid)), fp8mqa::kTopkThreads, 0,
+                          static_cast<cudaStream_t>(stream)>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return FP8MQA_ERR_LAUNCH;
+    return FP8MQA_OK;
 }
 
 const char* fp8_mqa_logits_strerror(int status)

@@ -164,6 +164,33 @@ FP8MQA_API int fp8_mqa_logits_noalloc(const uint8_t* q_fp8, const uint8_t* k_fp8
                                       int32_t H, int32_t D, int32_t clean_logits,
                                       int32_t split_n, void* stream);
 
+/*
+ * fp8_mqa_topk -- per-row top-k over a logits matrix, the step that consumes the indexer
+ * logits (ROCm/aiter PR #7183 "[HIP] [JIT] Add gfx950 prefill FP8 MQA logits", "Test plan":
+ * top-512 selections compared end to end; ROCm/aiter PR #6159 "[Triton/Gluon] GFX950 sparse
+ * mla optimizations", "Technical Details": sparse MLA with top-k 512).  The pages fix no tie
+ * rule or padding; this library reads the step as:
+ *   - only finite entries are eligible (-inf, a key outside the row's window, never is);
+ *   - row m's result lists its k largest eligible entries by value, descending, and equal
+ *     values by index, ascending (-0.0 equals +0.0);
+ *   - slots past the row's eligible entries hold index -1 and value -inf.
+ * The result is therefore unique.
+ *
+ *   logits   DEVICE float32, row m at logits + m * ld (ld >= N), 4-byte aligned; typically
+ *            the `out` of fp8_mqa_logits with clean_logits = 1.  Not modified.
+ *   M, N     rows and entries per row (M >= 0, 0 <= N <= 2^30).  M = 0 enqueues nothing.
+ *   k        1 <= k <= 2048.
+ *   indices  DEVICE int32 [M, k], row-major, 4-byte aligned, written.
+ *   values   DEVICE float32 [M, k] or NULL; when given, the selected logits (their exact
+ *            bits), -inf in padded slots.
+ *   stream   cudaStream_t; asynchronous.
+ * Errors: FP8MQA_ERR_INVALID_ARG (sizes, k, null pointers), FP8MQA_ERR_UNSUPPORTED_SHAPE
+ * (N too large), FP8MQA_ERR_MISALIGNED, FP8MQA_ERR_ARCH, FP8MQA_ERR_LAUNCH.  The first call on
+ * a device sets up the same per-device state as fp8_mqa_logits.
+ */
+FP8MQA_API int fp8_mqa_topk(const float* logits, int64_t M, int64_t N, int64_t ld, int32_t k,
+                            int32_t* indices, float* values, void* stream);
+
 /* fp8_mqa_logits_strerror -- a static, human-readable name for a status code. */
 FP8MQA_API const char* fp8_mqa_logits_strerror(int status);
 

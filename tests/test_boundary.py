@@ -22,7 +22,7 @@ def lib():
 
 def header_functions():
     text = open(HEADER).read()
-    return re.findall(r"FP8MQA_API\s+[\w\s\*]+?\b(fp8_mqa_logits\w*)\s*\(", text)
+    return re.findall(r"FP8MQA_API\s+[\w\s\*]+?\b(fp8_mqa_\w+)\s*\(", text)
 
 
 def test_header_declares_expected_entry_points():
@@ -119,3 +119,19 @@ def test_binding_rejects_cpu_tensors(lib):
     with pytest.raises(TypeError):
         fm.fp8_mqa_logits(q.view(torch.uint8), k, torch.ones(8), torch.ones(4, 32),
                           torch.zeros(4, dtype=torch.int32), torch.ones(4, dtype=torch.int32))
+
+
+def test_topk_rejects_bad_arguments_before_device_work(lib):
+    p = 0x1000
+    f = lib.fp8_mqa_topk
+    assert f(p, 0, 10, 10, 5, p, p, None) == 0                     # no rows: nothing to do
+    assert f(p, 4, 10, 10, 0, p, p, None) == -1
+    assert f(p, 4, 10, 10, 2049, p, p, None) == -1
+    assert f(p, 4, 10, 9, 5, p, p, None) == -1  # ld < N
+    assert f(p, -1, 10, 10, 5, p, p, None) == -1
+    assert f(None, 4, 10, 10, 5, p, p, None) == -1
+    assert f(p, 4, 10, 10, 5, None, p, None) == -1
+    assert f(p, 4, (1 << 30) + 1, (1 << 30) + 1, 5, p, p, None) == \
+        -2
+    assert f(p + 2, 4, 10, 10, 5, p, p, None) == -3
+    assert f(p, 4, 10, 10, 5, p, p + 1, None) == -3

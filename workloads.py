@@ -132,3 +132,19 @@ def valid_pairs(ks: np.ndarray, ke: np.ndarray, N: int) -> int:
     lo = np.clip(ks.astype(np.int64), 0, N)
     hi = np.clip(ke.astype(np.int64), 0, N)
     return int(np.maximum(hi - lo, 0).sum())
+
+
+def draw_logits(M: int, N: int, seed: int, ties: bool = True, neg_inf_frac: float = 0.25,
+                empty_rows: int = 1):
+    """Seeded float32 [M, N] logit-like rows for the top-k selection: N(0.5, 0.5) values, a
+    share of exact ties (values rounded to 1/8 on every 5th key), -inf on a random share of
+    keys, the first ``empty_rows`` rows all -inf, and a row of equal values."""
+    rng = np.random.default_rng(seed)
+    x = (0.5 + 0.5 * rng.standard_normal((M, N))).astype(np.float32)
+    if ties:
+        x[:, ::5] = np.round(x[:, ::5] * 8.0) / 8.0
+    x[rng.random((M, N)) < neg_inf_frac] = -np.inf
+    x[:min(M, empty_rows)] = -np.inf
+    if M > empty_rows + 1:
+        x[empty_rows + 1] = 0.75
+    return x
