@@ -75,7 +75,9 @@ void init_device(int dev, DeviceState& st)
         return;
     }
     if (cudaFuncSetAttribute(fp8_mqa_logits_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             int(kSmemBytes)) != cudaSuccess) {
+                             int(kSmemBytes)) != cudaSuccess ||
+        cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(kTopkSmemBytes)) != cudaSuccess) {
         st.init_status = FP8MQA_ERR_LAUNCH;
         return;
     }
@@ -456,7 +458,7 @@ int fp8_mqa_topk(const float* logits, int64_t M, int64_t N, int64_t ld, int32_t 
     // one CTA per SM, each walking rows: the rows in flight stay resident in L2 for the
     // select's re-reads
     const int64_t grid = M < st->sm_count ? M : st->sm_count;
-    fp8mqa::topk_kernel<<<dim3(uint32_t(grid)), fp8mqa::kTopkThreads, 0,
+    fp8mqa::topk_kernel<<<dim3(uint32_t(grid)), fp8mqa::kTopkThreads, fp8mqa::kTopkSmemBytes,
                           static_cast<cudaStream_t>(stream)>>>(p);
     if (cudaGetLastError() != cudaSuccess) return FP8MQA_ERR_LAUNCH;
     return FP8MQA_OK;

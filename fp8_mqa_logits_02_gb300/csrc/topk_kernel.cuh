@@ -7,11 +7,18 @@
 // selected), ordered by value descending and, for equal values, by index ascending (-0.0
 // equals +0.0); slots past the row's finite entries get index -1 and value -inf.
 //
-// One CTA per row at a time (persistent grid of one CTA per SM, so a row's re-reads come
-// from L2).  Radix select on an order-preserving 32-bit key: three histogram passes of
-// 11, 11 and 10 bits find the exact k-th key T and how many of the entries equal to T are
-// taken; a collect pass gathers the entries above T and, in index order, the needed ties;
-// a bitonic sort in shared memory orders the (at most 2048) winners.
+// One CTA per row at a time (persistent grid of one CTA per SM, so a row's second read
+// comes from L2).  Radix select on an order-preserving 32-bit key:
+//   1. read the row, histogram the top 11 key bits (a private histogram per warp, so hot
+//      bins do not serialise the whole block);
+//   2. the bin b0 holding the k-th largest is found from the top;
+//   3. read the row again: keys above b0 go straight to the winners, keys in b0 to a
+//      shared-memory buffer, where two more radix passes (key bits 20..10 and 9..0) pick
+//      the rest and equal keys are taken by index;
+//   4. the winners (at most 2048) are sorted by a bitonic network and written.
+// When b0 holds more entries than the buffer, the remaining 21 key bits are resolved by
+// two more histogram passes over the row and a collect pass that takes the ties in index
+// order.
 #pragma once
 
 #include <cstdint>
@@ -21,7 +28,8 @@ namespace fp8mqa {
 constexpr int kTopkThreads = 512;
 constexpr int kTopkWarps = kTopkThreads / 32;
 constexpr int kTopkMaxK = 2048;
-constexpr int kTopkBins = 2048;  // 11-bit digits
+constexpr int kTopkBins = 2048;      // 11-bit digits
+constexpr int kTopkTieCap = 8192;    // entries of the threshold bin sorted in shared memory
 
 struct TopkParams {
     const float* logits;
@@ -30,6 +38,17 @@ struct TopkParams {
     int32_t* indices;  // [M, k]
     float* values;     // [M, k] or null
 };
+
+struct TopkSmem {
+    uint32_t whist[kTopkWarps][kTopkBins];
+    uint32_t hist[kTopkBins];
+    unsigned long long cand[kTopkMaxK];
+    unsigned long long tbuf[kTopkTieCap];
+    uint32_t scratch[kTopkWarps];
+    uint32_t sel_bin, sel_above, sel_count, n_cand, n_tie, tie_base;
+};
+constexpr uint32_t kTopkSmemBytes = sizeof(TopkSmem);
+static_assert(kTopkSmemBytes <= 232448, "top-k shared memory");
 
 // Order-preserving key of a finite float (larger value, larger key; -0.0 and +0.0 equal).
 __device__ __forceinline__ uint32_t topk_key(float x)
@@ -42,6 +61,12 @@ __device__ __forceinline__ uint32_t topk_key(float x)
 __device__ __forceinline__ bool topk_eligible(float x)
 {
     return (__float_as_uint(x) & 0x7F800000u) != 0x7F800000u;  // finite
+}
+
+// Winners sort by this value, descending: key first, then the lower index.
+__device__ __forceinline__ unsigned long long topk_composite(uint32_t key, int i)
+{
+    return (static_cast<unsigned long long>(key) << 32) | (0xFFFFFFFFu - uint32_t(i));
 }
 
 // Block-wide inclusive sum over threads in index order; `scratch` holds kTopkWarps words.
@@ -67,152 +92,294 @@ __device__ __forceinline__ uint32_t topk_block_scan(uint32_t v, uint32_t* scratc
     return v + before;
 }
 
+// Visit every element of the row once, in chunks whose trip count is uniform over the block
+// (so warp votes inside `fn` see every lane): fn(index, value, valid).  16-byte aligned rows
+// are read four floats per thread per chunk unless kInOrder asks for one element per thread
+// per call, so that successive calls cover the row in index order.
+template <bool kInOrder = false, typename Fn>
+__device__ __forceinline__ void topk_for_row(const float* x, int N, Fn&& fn)
+{
+    const int tid = threadIdx.x;
+    if (!kInOrder && (reinterpret_cast<uintptr_t>(x) & 15u) == 0) {
+        // four 16-byte loads in flight per thread before any is used
+        constexpr int kU = 4;
+        for (int c0 = 0; c0 < N; c0 += 4 * kU * kTopkThreads) {
+            float4 v[kU];
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                const int i = c0 + 4 * (u * kTopkThreads + tid);
+                v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (i + 3 < N) {
+                    v[u] = __ldg(reinterpret_cast<const float4*>(x + i));
+                } else {
+                    if (i < N) v[u].x = __ldg(x + i);
+                    if (i + 1 < N) v[u].y = __ldg(x + i + 1);
+                    if (i + 2 < N) v[u].z = __ldg(x + i + 2);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                const int i = c0 + 4 * (u * kTopkThreads + tid);
+                fn(i, v[u].x, i < N);
+                fn(i + 1, v[u].y, i + 1 < N);
+                fn(i + 2, v[u].z, i + 2 < N);
+                fn(i + 3, v[u].w, i + 3 < N);
+            }
+        }
+    } else {
+        for (int c0 = 0; c0 < N; c0 += kTopkThreads) {
+            const int i = c0 + tid;
+            fn(i, i < N ? __ldg(x + i) : 0.f, i < N);
+        }
+    }
+}
+
+// Add one to hist[bin] for every lane with `in`.
+__device__ __forceinline__ void topk_hist_add(uint32_t* hist, uint32_t bin, bool in)
+{
+    if (in) atomicAdd(&hist[bin], 1u);
+}
+
+// Append `v` for every lane with `take` to buf[*count...], one atomic per warp.
+__device__ __forceinline__ void topk_append(unsigned long long* buf, uint32_t* count,
+                                            unsigned long long v, bool take)
+{
+    const uint32_t mask = __ballot_sync(0xffffffffu, take);
+    if (mask == 0) return;
+    const int lane = threadIdx.x & 31;
+    const int leader = __ffs(mask) - 1;
+    uint32_t base = 0;
+    if (lane == leader) base = atomicAdd(count, uint32_t(__popc(mask)));
+    base = __shfl_sync(0xffffffffu, base, leader);
+    if (take) buf[base + __popc(mask & ((1u << lane) - 1u))] = v;
+}
+
+// The bin holding the kk-th largest entry, scanning hist[0, nb) from the top; writes
+// sel_bin, sel_above (entries in higher bins) and sel_count (entries in the bin).  Returns
+// the total count.  Uniform over the block.
+__device__ __forceinline__ uint32_t topk_find_bin(TopkSmem& s, const uint32_t* hist, uint32_t nb,
+                                                  uint32_t kk)
+{
+    const int tid = threadIdx.x;
+    const int per = int(nb) / kTopkThreads;
+    uint32_t run = 0;
+    for (int j = 0; j < per; ++j) run += hist[nb - 1 - (tid * per + j)];
+    uint32_t total = 0;
+    const uint32_t incl = topk_block_scan(run, s.scratch, total);
+    const uint32_t excl = incl - run;
+    if (kk <= total && excl < kk && incl >= kk) {
+        uint32_t above = excl;
+        for (int j = 0; j < per; ++j) {
+            const uint32_t b = nb - 1 - (tid * per + j);
+            const uint32_t h = hist[b];
+            if (above + h >= kk) {
+                s.sel_bin = b;
+                s.sel_above = above;
+                s.sel_count = h;
+                break;
+            }
+            above += h;
+        }
+    }
+    __syncthreads();
+    return total;
+}
+
+// Bitonic sort of buf[0, n) descending (padding with zeros up to a power of two <= cap).
+__device__ __forceinline__ void topk_sort_desc(unsigned long long* buf, int n);
+
+// Move the kk largest composites of buf[0, n) (all with the same top 11 key bits) to the
+// winners.  Two radix passes over the buffer, on key bits 20..10 and 9..0, narrow it to the
+// entries whose key equals the kk-th largest key; of those, the ones with the lowest index
+// are taken (a sort of just these ties when the cut falls inside them).  `spare` holds at
+// least n composites.
+__device__ __forceinline__ void topk_select_buffer(TopkSmem& s, unsigned long long* buf,
+                                                   unsigned long long* spare, uint32_t n,
+                                                   uint32_t kk)
+{
+    const int tid = threadIdx.x;
+    for (int pass = 0; pass < 2; ++pass) {
+        const int shift = pass == 0 ? 10 : 0;
+        const uint32_t nb = pass == 0 ? 2048u : 1024u;
+        for (uint32_t b = tid; b < nb; b += kTopkThreads) s.hist[b] = 0;
+        if (tid == 0) s.n_tie = 0;
+        __syncthreads();
+        for (uint32_t j = tid; j < n; j += kTopkThreads)
+            atomicAdd(&s.hist[uint32_t(buf[j] >> (32 + shift)) & (nb - 1)], 1u);
+        __syncthreads();
+        topk_find_bin(s, s.hist, nb, kk);
+        const uint32_t b = s.sel_bin;
+        kk -= s.sel_above;
+        // entries above the bin are winners; the bin's entries move on to the next pass
+        const uint32_t rounds = (n + kTopkThreads - 1) / kTopkThreads;
+        for (uint32_t r = 0; r < rounds; ++r) {
+            const uint32_t j = r * kTopkThreads + tid;
+            const unsigned long long c = j < n ? buf[j] : 0ull;
+            const uint32_t d = uint32_t(c >> (32 + shift)) & (nb - 1);
+            topk_append(s.cand, &s.n_cand, c, j < n && d > b);
+            topk_append(spare, &s.n_tie, c, j < n && d == b);
+        }
+        __syncthreads();
+        n = s.n_tie;
+        unsigned long long* t = buf;
+        buf = spare;
+        spare = t;
+        __syncthreads();  // every thread has read n before the next pass resets the count
+    }
+    // buf[0, n) now holds the entries equal to the kk-th largest key; take kk by index
+    if (kk < n) topk_sort_desc(buf, int(n));
+    for (uint32_t j = tid; j < kk; j += kTopkThreads) {
+        // the composite orders equal keys by index, so after the sort these are the lowest
+        s.cand[s.n_cand + j] = buf[j];
+    }
+    __syncthreads();
+    if (tid == 0) s.n_cand += kk;
+    __syncthreads();
+}
+
+// Bitonic sort of buf[0, n) descending (padding with zeros up to a power of two <= cap).
+__device__ __forceinline__ void topk_sort_desc(unsigned long long* buf, int n)
+{
+    const int tid = threadIdx.x;
+    int P = 1;
+    while (P < n) P <<= 1;
+    for (int i = n + tid; i < P; i += kTopkThreads) buf[i] = 0ull;
+    __syncthreads();
+    for (int size = 2; size <= P; size <<= 1) {
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            for (int t = tid; t < P / 2; t += kTopkThreads) {
+                const int lo = (t / stride) * stride * 2 + (t % stride);
+                const int hi = lo + stride;
+                const bool desc = (lo & size) == 0;
+                const unsigned long long a = buf[lo], b = buf[hi];
+                if ((a < b) == desc) {
+                    buf[lo] = b;
+                    buf[hi] = a;
+                }
+            }
+            __syncthreads();
+        }
+    }
+}
+
 __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkParams p)
 {
-    __shared__ uint32_t hist[kTopkBins];
-    __shared__ unsigned long long cand[kTopkMaxK];
-    __shared__ uint32_t scratch[kTopkWarps];
-    __shared__ uint32_t sel_bin, sel_above, n_cand, tie_base;
-
-    const int tid = threadIdx.x, lane = tid & 31;
+    extern __shared__ __align__(16) uint8_t topk_smem_raw[];
+    TopkSmem& s = *reinterpret_cast<TopkSmem*>(topk_smem_raw);
+    const int tid = threadIdx.x, warp = tid >> 5;
     const int N = int(p.N);
     const int k = p.k;
+    uint32_t* const my_hist = s.whist[warp];
 
     for (int64_t row = blockIdx.x; row < p.M; row += gridDim.x) {
         const float* x = p.logits + row * p.ld;
 
-        // ---- radix select: find the k-th largest key T and how many entries equal to T
-        uint32_t prefix = 0, pmask = 0;
-        int kk = k;              // entries still to take among those matching the prefix
-        uint32_t tie_total = 0;  // entries equal to T
-        bool take_all = false;   // fewer than k eligible entries: take every one
-        for (int pass = 0; pass < 3; ++pass) {
-            const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
-            const int width = pass < 2 ? 11 : 10;
-            const uint32_t nb = 1u << width;
-            for (uint32_t b = tid; b < nb; b += kTopkThreads) hist[b] = 0;
-            __syncthreads();
-            // a trip count uniform over the block, so the warp votes below see every lane
-            for (int c0 = 0; c0 < N; c0 += kTopkThreads) {
-                const int i = c0 + tid;
-                const float v = i < N ? x[i] : __int_as_float(0xff800000);
-                bool in = topk_eligible(v);
-                uint32_t bin = 0;
-                if (in) {
-                    const uint32_t key = topk_key(v);
-                    in = (key & pmask) == prefix;
-                    bin = (key >> shift) & (nb - 1);
-                }
-                // one shared-memory atomic per distinct bin in the warp
-                const uint32_t act = __ballot_sync(0xffffffffu, in);
-                if (in) {
-                    const uint32_t peers = __match_any_sync(act, bin);
-                    if (lane == __ffs(peers) - 1) atomicAdd(&hist[bin], uint32_t(__popc(peers)));
-                }
-            }
-            __syncthreads();
-            // the bin holding the kk-th largest, scanning from the top: each thread owns a
-            // run of nb / kTopkThreads bins, highest bins at thread 0
-            const int per = int(nb) / kTopkThreads;
-            uint32_t run = 0;
-            for (int j = 0; j < per; ++j) run += hist[nb - 1 - (tid * per + j)];
-            uint32_t total = 0;
-            const uint32_t incl = topk_block_scan(run, scratch, total);
-            if (pass == 0 && total <= uint32_t(k)) {
-                take_all = true;
-                break;
-            }
-            const uint32_t excl = incl - run;
-            if (excl < uint32_t(kk) && incl >= uint32_t(kk)) {
-                uint32_t above = excl;
-                for (int j = 0; j < per; ++j) {
-                    const uint32_t b = nb - 1 - (tid * per + j);
-                    const uint32_t h = hist[b];
-                    if (above + h >= uint32_t(kk)) {
-                        sel_bin = b;
-                        sel_above = above;
-                        tie_base = h;
-                        break;
-                    }
-                    above += h;
-                }
-            }
-            __syncthreads();
-            kk -= int(sel_above);
-            prefix |= sel_bin << shift;
-            pmask |= (nb - 1) << shift;
-            tie_total = tie_base;
-            __syncthreads();
+        // ---- 1. top 11 key bits, one histogram per warp, then their sum
+        for (int b = tid & 31; b < kTopkBins; b += 32) my_hist[b] = 0;
+        __syncwarp();
+        topk_for_row(x, N, [&](int, float v, bool valid) {
+            const bool in = valid && topk_eligible(v);
+            topk_hist_add(my_hist, in ? (topk_key(v) >> 21) : 0u, in);
+        });
+        __syncthreads();
+        for (int b = tid; b < kTopkBins; b += kTopkThreads) {
+            uint32_t h = 0;
+#pragma unroll
+            for (int w = 0; w < kTopkWarps; ++w) h += s.whist[w][b];
+            s.hist[b] = h;
         }
-        const uint32_t T = prefix;
-        // ties need index order only when the cut falls inside them
-        const bool ordered_ties = !take_all && uint32_t(kk) < tie_total;
-
-        // ---- collect the winners (unordered), ties in index order when needed
         if (tid == 0) {
-            n_cand = 0;
-            tie_base = 0;
+            s.n_cand = 0;
+            s.n_tie = 0;
+            s.tie_base = 0;
         }
         __syncthreads();
-        for (int c0 = 0; c0 < N; c0 += kTopkThreads) {
-            const int i = c0 + tid;
-            bool greater = false, tie = false;
-            uint32_t key = 0;
-            if (i < N) {
-                const float v = x[i];
-                if (topk_eligible(v)) {
-                    key = topk_key(v);
-                    greater = take_all || key > T;
-                    tie = !take_all && key == T;
-                }
-            }
-            bool take = greater || (tie && !ordered_ties);
-            if (ordered_ties) {
-                // rank of this tie among all ties of the row, in index order
-                uint32_t chunk_ties = 0;
-                const uint32_t incl = topk_block_scan(tie ? 1u : 0u, scratch, chunk_ties);
-                const uint32_t rank = tie_base + incl - (tie ? 1u : 0u);
-                take = greater || (tie && rank < uint32_t(kk));
-                __syncthreads();
-                if (tid == 0) tie_base += chunk_ties;
-            }
-            if (take) {
-                const uint32_t slot = atomicAdd(&n_cand, 1u);
-                cand[slot] = (static_cast<unsigned long long>(key) << 32) | (0xFFFFFFFFu - uint32_t(i));
-            }
-        }
-        __syncthreads();
-        const int n_sel = int(n_cand);
 
-        // ---- bitonic sort, descending on (key, -index)
-        int P = 1;
-        while (P < n_sel) P <<= 1;
-        for (int i = n_sel + tid; i < P; i += kTopkThreads) cand[i] = 0ull;
-        __syncthreads();
-        for (int size = 2; size <= P; size <<= 1) {
-            for (int stride = size >> 1; stride > 0; stride >>= 1) {
-                for (int t = tid; t < P / 2; t += kTopkThreads) {
-                    const int lo = (t / stride) * stride * 2 + (t % stride);
-                    const int hi = lo + stride;
-                    const bool desc = (lo & size) == 0;
-                    const unsigned long long a = cand[lo], b = cand[hi];
-                    if ((a < b) == desc) {
-                        cand[lo] = b;
-                        cand[hi] = a;
-                    }
-                }
+        // ---- 2. the bin of the k-th largest
+        const uint32_t total = topk_find_bin(s, s.hist, kTopkBins, uint32_t(k));
+        const bool take_all = total <= uint32_t(k);
+        const uint32_t b0 = s.sel_bin, above0 = s.sel_above, count0 = s.sel_count;
+        const bool fast = take_all || count0 <= uint32_t(kTopkTieCap);
+
+        if (fast) {
+            // ---- 3. winners above b0, the b0 entries into the buffer
+            topk_for_row(x, N, [&](int i, float v, bool valid) {
+                const bool in = valid && topk_eligible(v);
+                const uint32_t key = in ? topk_key(v) : 0u;
+                const uint32_t d = key >> 21;
+                const unsigned long long c = topk_composite(key, i);
+                topk_append(s.cand, &s.n_cand, c, in && (take_all || d > b0));
+                topk_append(s.tbuf, &s.n_tie, c, in && !take_all && d == b0);
+            });
+            __syncthreads();
+            if (!take_all) {
+                // the kk largest of the b0 entries, ties by index; the per-warp histograms
+                // are free now and hold the spare buffer
+                topk_select_buffer(s, s.tbuf, reinterpret_cast<unsigned long long*>(&s.whist[0][0]),
+                                   s.n_tie, uint32_t(k) - above0);
+            }
+        } else {
+            // ---- 3'. the threshold bin is too large for the buffer: resolve the other 21
+            // key bits with two more histogram passes (10 and 11 bits)
+            uint32_t prefix = b0 << 21, pmask = 0x7FFu << 21;
+            uint32_t kk = uint32_t(k) - above0;
+            uint32_t tie_total = count0;
+            for (int pass = 1; pass < 3; ++pass) {
+                const int shift = pass == 1 ? 10 : 0;
+                const uint32_t nb = pass == 1 ? 2048u : 1024u;
+                for (uint32_t b = tid; b < nb; b += kTopkThreads) s.hist[b] = 0;
+                __syncthreads();
+                topk_for_row(x, N, [&](int, float v, bool valid) {
+                    bool in = valid && topk_eligible(v);
+                    const uint32_t key = in ? topk_key(v) : 0u;
+                    in = in && (key & pmask) == prefix;
+                    topk_hist_add(s.hist, (key >> shift) & (nb - 1), in);
+                });
+                __syncthreads();
+                topk_find_bin(s, s.hist, nb, kk);
+                kk -= s.sel_above;
+                prefix |= s.sel_bin << shift;
+                pmask |= (nb - 1) << shift;
+                tie_total = s.sel_count;
                 __syncthreads();
             }
+            const uint32_t T = prefix;  // the k-th largest key; kk of the entries equal to it
+            const bool ordered_ties = kk < tie_total;
+            auto collect = [&](int i, float v, bool valid) {
+                const bool in = valid && topk_eligible(v);
+                const uint32_t key = in ? topk_key(v) : 0u;
+                const bool greater = in && key > T;
+                const bool tie = in && key == T;
+                bool take = greater || (tie && !ordered_ties);
+                if (ordered_ties) {
+                    // rank of this tie among the row's ties, in index order (the in-order
+                    // visit gives one element per thread per call, threads in index order)
+                    uint32_t step_ties = 0;
+                    const uint32_t incl = topk_block_scan(tie ? 1u : 0u, s.scratch, step_ties);
+                    const uint32_t rank = s.tie_base + incl - (tie ? 1u : 0u);
+                    take = greater || (tie && rank < kk);
+                    __syncthreads();
+                    if (tid == 0) s.tie_base += step_ties;
+                }
+                topk_append(s.cand, &s.n_cand, topk_composite(key, i), take);
+            };
+            if (ordered_ties)
+                topk_for_row<true>(x, N, collect);
+            else
+                topk_for_row(x, N, collect);
+            __syncthreads();
         }
 
-        // ---- write the row
+        // ---- 4. order the winners and write the row
+        const int n_sel = int(s.n_cand);
+        topk_sort_desc(s.cand, n_sel);
         int32_t* oi = p.indices + row * int64_t(k);
         float* ov = p.values ? p.values + row * int64_t(k) : nullptr;
         for (int j = tid; j < k; j += kTopkThreads) {
             int32_t idx = -1;
             float val = __int_as_float(0xff800000);
             if (j < n_sel) {
-                idx = int32_t(0xFFFFFFFFu - uint32_t(cand[j] & 0xFFFFFFFFull));
+                idx = int32_t(0xFFFFFFFFu - uint32_t(s.cand[j] & 0xFFFFFFFFull));
                 val = x[idx];
             }
             oi[j] = idx;

@@ -94,3 +94,18 @@ def test_indexer_pipeline_top512_matches_the_oracle_pipeline():
     same = sum(set(a.tolist()) == set(b.tolist()) for a, b in zip(gi, ri))
     overlap = min(len(set(a.tolist()) & set(b.tolist())) for a, b in zip(gi, ri))
     assert same >= 0.9 * len(rows) and overlap >= 500, (same, overlap)
+
+
+def test_crowded_threshold_bin_takes_the_multi_pass_path():
+    # more than 8192 entries share the top 11 key bits of the k-th largest: the select
+    # resolves the remaining bits with further passes over the row
+    N = 20000
+    x = np.empty((5, N), dtype=np.float32)
+    x[0] = 1.0                                            # all equal: ties in index order
+    x[1] = 1.0 + np.arange(N, dtype=np.float32) * 2.0 ** -23   # distinct, one top bin
+    x[2] = x[1][::-1]
+    x[3] = 1.0
+    x[3, 7::13] = 1.0 + 2.0 ** -20                        # a few slightly larger ones first
+    x[4] = 1.0 + (np.arange(N) % 97).astype(np.float32) * 2.0 ** -23   # many tie groups
+    for k in (1, 5, 100, 1537, 2048):
+        _check(x, k, what=f"crowded k={k}")
