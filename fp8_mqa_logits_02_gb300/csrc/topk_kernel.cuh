@@ -187,6 +187,8 @@ __device__ __forceinline__ uint32_t topk_find_bin(TopkSmem& s, const uint32_t* h
 
 // Bitonic sort of buf[0, n) descending (padding with zeros up to a power of two <= cap).
 __device__ __forceinline__ void topk_sort_desc(unsigned long long* buf, int n);
+// Descending sort of buf[0, n), fastest network for n.
+__device__ __forceinline__ void topk_sort_any(unsigned long long* buf, int n);
 
 // Move the kk largest composites of buf[0, n) (all with the same top 11 key bits) to the
 // winners.  Two radix passes over the buffer, on key bits 20..10 and 9..0, narrow it to the
@@ -227,7 +229,7 @@ __device__ __forceinline__ void topk_select_buffer(TopkSmem& s, unsigned long lo
         __syncthreads();  // every thread has read n before the next pass resets the count
     }
     // buf[0, n) now holds the entries equal to the kk-th largest key; take kk by index
-    if (kk < n) topk_sort_desc(buf, int(n));
+    if (kk < n) topk_sort_any(buf, int(n));
     for (uint32_t j = tid; j < kk; j += kTopkThreads) {
         // the composite orders equal keys by index, so after the sort these are the lowest
         s.cand[s.n_cand + j] = buf[j];
@@ -260,6 +262,94 @@ __device__ __forceinline__ void topk_sort_desc(unsigned long long* buf, int n)
             __syncthreads();
         }
     }
+}
+
+// One compare-exchange step at stride S < E between a thread's own elements (S fixed at
+// compile time so the elements stay in registers).
+template <int E, int S>
+__device__ __forceinline__ void topk_sort_in_thread(unsigned long long (&v)[E], int tid, int size)
+{
+    if constexpr (S < E) {
+#pragma unroll
+        for (int j = 0; j < E; ++j) {
+            if (j & S) continue;
+            const bool desc = ((tid * E + j) & size) == 0;
+            const unsigned long long a = v[j], b = v[j | S];
+            if ((a < b) == desc) {
+                v[j] = b;
+                v[j | S] = a;
+            }
+        }
+    }
+}
+
+// Bitonic sort of buf[0, n) descending for n <= 512 * E, with thread t holding elements
+// t*E .. t*E+E-1 in registers: compare-exchanges at strides below E stay in the thread, at
+// strides below 32*E use warp shuffles, and only the wider ones go through shared memory
+// (two barriers each).
+template <int E>
+__device__ __forceinline__ void topk_sort_desc_reg(unsigned long long* buf, int n)
+{
+    constexpr int P = kTopkThreads * E;
+    const int tid = threadIdx.x;
+    unsigned long long v[E];
+#pragma unroll
+    for (int j = 0; j < E; ++j) {
+        const int e = tid * E + j;
+        v[j] = e < n ? buf[e] : 0ull;
+    }
+    __syncthreads();
+    for (int size = 2; size <= P; size <<= 1) {
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            if (stride >= 32 * E) {
+#pragma unroll
+                for (int j = 0; j < E; ++j) buf[tid * E + j] = v[j];
+                __syncthreads();
+#pragma unroll
+                for (int j = 0; j < E; ++j) {
+                    const int e = tid * E + j;
+                    const unsigned long long o = buf[e ^ stride];
+                    const bool desc = (e & size) == 0, lo = (e & stride) == 0;
+                    const bool keep_max = desc == lo;
+                    v[j] = keep_max ? (v[j] > o ? v[j] : o) : (v[j] < o ? v[j] : o);
+                }
+                __syncthreads();
+            } else if (stride >= E) {
+                const int lanes = stride / E;
+#pragma unroll
+                for (int j = 0; j < E; ++j) {
+                    const int e = tid * E + j;
+                    const unsigned long long o = __shfl_xor_sync(0xffffffffu, v[j], lanes);
+                    const bool desc = (e & size) == 0, lo = (e & stride) == 0;
+                    const bool keep_max = desc == lo;
+                    v[j] = keep_max ? (v[j] > o ? v[j] : o) : (v[j] < o ? v[j] : o);
+                }
+            } else if (stride == 1) {
+                topk_sort_in_thread<E, 1>(v, tid, size);
+            } else {
+                topk_sort_in_thread<E, 2>(v, tid, size);
+            }
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < E; ++j) {
+        const int e = tid * E + j;
+        if (e < n) buf[e] = v[j];
+    }
+    __syncthreads();
+}
+
+// Descending sort of buf[0, n): in registers up to 2048 entries, else in shared memory.
+__device__ __forceinline__ void topk_sort_any(unsigned long long* buf, int n)
+{
+    if (n <= kTopkThreads)
+        topk_sort_desc_reg<1>(buf, n);
+    else if (n <= 2 * kTopkThreads)
+        topk_sort_desc_reg<2>(buf, n);
+    else if (n <= 4 * kTopkThreads)
+        topk_sort_desc_reg<4>(buf, n);
+    else
+        topk_sort_desc(buf, n);
 }
 
 __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkParams p)
@@ -372,7 +462,7 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkParams 
 
         // ---- 4. order the winners and write the row
         const int n_sel = int(s.n_cand);
-        topk_sort_desc(s.cand, n_sel);
+        topk_sort_any(s.cand, n_sel);
         int32_t* oi = p.indices + row * int64_t(k);
         float* ov = p.values ? p.values + row * int64_t(k) : nullptr;
         for (int j = tid; j < k; j += kTopkThreads) {
