@@ -324,15 +324,19 @@ int fp8_mqa_logits_is_supported(int64_t M, int64_t N, int32_t H, int32_t D)
 
 int fp8_mqa_logits_default_split(int64_t M, int64_t N, int32_t num_sms)
 {
-    // Enough units for the dynamic scheduler to balance the tail: about 8 per SM, or 16
-    // when there are fewer than two row blocks per SM (then every block is split into many
+    // Enough units for the dynamic scheduler to balance the tail, and no more: every unit
+    // costs a claim, a Q load and a pipeline restart.  About 4 units per SM when there are
+    // four or more row blocks per SM (heaviest-first order then balances whole blocks), 8
+    // below that, and 16 under two blocks per SM (every block is then split into many
     // chunks of equal work and the last chunks decide the finish).  Chunks keep at least 8
-    // key tiles so Q reloads and per-unit costs stay small.
+    // key tiles.
     if (M <= 0 || N <= 0) return 1;
     if (num_sms < 1) num_sms = 1;
     const int64_t tiles = (N + fp8mqa::kTileKeys - 1) / fp8mqa::kTileKeys;
     const int64_t blocks = (M + fp8mqa::kRows - 1) / fp8mqa::kRows;
-    const int64_t target = int64_t(blocks < 2 * int64_t(num_sms) ? 16 : 8) * num_sms;
+    const int64_t sms = num_sms;
+    const int64_t per_sm = blocks < 2 * sms ? 16 : (blocks < 4 * sms ? 8 : 4);
+    const int64_t target = per_sm * sms;
     int64_t s = (target + blocks - 1) / blocks;
     const int64_t cap = tiles / 8 > 1 ? tiles / 8 : 1;
     if (s > cap) s = cap;

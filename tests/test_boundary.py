@@ -60,9 +60,10 @@ def test_is_supported_truth_table(lib):
 
 
 def test_default_split(lib):
-    # about 8 units per SM (16 when there are under two row blocks per SM), chunks of at
-    # least 8 key tiles
-    assert fm.default_split(8192, 8192, 152) == 2
+    # about 4, 8 or 16 units per SM for many, some or few row blocks; chunks of at least
+    # 8 key tiles
+    assert fm.default_split(8192, 8192, 152) == 1
+    assert fm.default_split(16384, 32000, 152) == 1
     assert fm.default_split(4096, 32768, 152) == 3
     assert fm.default_split(1024, 131072, 152) == 19
     assert fm.default_split(64, 256, 152) == 1
