@@ -225,3 +225,28 @@ def test_call_captured_in_a_cuda_graph():
         torch.cuda.synchronize()
         assert fm.check_error() == 0
         assert_parity(out.cpu().numpy(), ref, inside, True, what="graph replay")
+
+
+# ------------------------------------------------------------------ randomized configurations
+def _random_config(rng):
+    M = int(rng.integers(1, 100))
+    N = int(rng.integers(1, 2000))
+    q, k, kv, w = workloads.draw(M, N, int(rng.integers(0, 1 << 30)))
+    # arbitrary per-row windows: negative starts, ends past N, empty and reversed rows
+    ks = rng.integers(-50, N + 50, size=M)
+    ke = ks + rng.integers(-20, N + 100, size=M)
+    return {"q": q, "k": k, "kv_scale": kv, "w": w, "ks": ks.astype(np.int32),
+            "ke": ke.astype(np.int32), "M": M, "N": N, "H": 32, "D": 128}
+
+
+@pytest.mark.parametrize("case", range(40))
+def test_randomized_configs(case):
+    rng = np.random.default_rng(1000 + case)
+    inp = _random_config(rng)
+    clean = bool(rng.integers(0, 2))
+    split = int(rng.choice([0, 1, 2, 3, 7, 50]))
+    gpu = run_gpu(inp, clean=clean, split_n=split)
+    ref = run_oracle(inp, clean=clean)
+    assert_parity(gpu, ref, window_mask(inp["ks"], inp["ke"], inp["N"]), clean,
+                  what=f"random case {case}: M={inp['M']} N={inp['N']} clean={clean} "
+                       f"split={split}")
