@@ -326,16 +326,16 @@ int fp8_mqa_logits_default_split(int64_t M, int64_t N, int32_t num_sms)
 {
     // Enough units for the dynamic scheduler to balance the tail, and no more: every unit
     // costs a claim, a Q load and a pipeline restart.  About 4 units per SM when there are
-    // four or more row blocks per SM (heaviest-first order then balances whole blocks), 8
-    // below that, and 16 under two blocks per SM (every block is then split into many
+    // four or more row blocks per SM (heaviest-first order then balances whole blocks), 20
+    // with two to four blocks per SM, and 16 under two (every block is then split into many
     // chunks of equal work and the last chunks decide the finish).  Chunks keep at least 8
-    // key tiles.
+    // key tiles; the kernel splits a block with narrow windows along its own tile range.
     if (M <= 0 || N <= 0) return 1;
     if (num_sms < 1) num_sms = 1;
     const int64_t tiles = (N + fp8mqa::kTileKeys - 1) / fp8mqa::kTileKeys;
     const int64_t blocks = (M + fp8mqa::kRows - 1) / fp8mqa::kRows;
     const int64_t sms = num_sms;
-    const int64_t per_sm = blocks < 2 * sms ? 16 : (blocks < 4 * sms ? 8 : 4);
+    const int64_t per_sm = blocks < 2 * sms ? 16 : (blocks < 4 * sms ? 20 : 4);
     const int64_t target = per_sm * sms;
     int64_t s = (target + blocks - 1) / blocks;
     const int64_t cap = tiles / 8 > 1 ? tiles / 8 : 1;

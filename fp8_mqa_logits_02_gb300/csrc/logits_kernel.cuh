@@ -6,7 +6,9 @@
 //
 // Work unit = (row block of kRows = 8 query rows, key chunk).  A persistent grid of one
 // CTA per SM pulls units from a global counter, heaviest row blocks first (the page's
-// "reverse_rows", section "Design / Grid choice"); key chunks are the page's SplitN.
+// "reverse_rows", section "Design / Grid choice"); key chunks are the page's SplitN.  A
+// block whose windows cover under half of the keys is chunked along its own tile range
+// instead (the page's layout-aware split for multi-request chunks, "Known limitations").
 //
 // Warp roles in a 640-thread CTA:
 //   warp 0      producer: claims units, computes each unit's key-tile range from the
@@ -270,10 +272,12 @@ __device__ __forceinline__ int64_t clamp64(int64_t v, int64_t lo, int64_t hi)
 struct Geometry {
     int32_t m0, t0, t1, ct0, ct1;
     int32_t ut0, ut1;  // key tiles meeting the union of the block's windows (empty: ut0 >= ut1)
+    int32_t skip;      // compute claims: chunks of this block before `skip` hold nothing more
     int32_t lo, hi;  // lane r < kRows: row m0 + r's window clamped to [0, N) (empty past M)
 };
 
-__device__ __forceinline__ Geometry unit_geometry(const Params& p, int32_t b, int32_t c)
+__device__ __forceinline__ Geometry unit_geometry(const Params& p, int32_t b, int32_t c,
+                                                  bool compute = false)
 {
     const int lane = threadIdx.x & 31;
     Geometry g;
@@ -305,13 +309,32 @@ __device__ __forceinline__ Geometry unit_geometry(const Params& p, int32_t b, in
     g.t1 = g.ct0;
     g.ut0 = 0;
     g.ut1 = 0;
+    g.skip = p.split;  // no tiles: every chunk of the block is empty
     if (lo < hi) {
         g.ut0 = int32_t(lo / kTileKeys);
         g.ut1 = int32_t((hi + kTileKeys - 1) / kTileKeys);
-        if (g.ct0 < g.ct1) {
-            g.t0 = max(g.ct0, g.ut0);
-            g.t1 = min(g.ct1, g.ut1);
-            if (g.t1 < g.t0) g.t1 = g.t0;
+        const int32_t len = g.ut1 - g.ut0;
+        if (compute && 2 * len < p.num_tiles) {
+            // A block whose windows cover under half of the keys (a request of a
+            // multi-request chunk, say) is split along its own tile range into equal chunks
+            // of at least 8 tiles, so it yields `split` units of work instead of mostly empty
+            // fixed chunks.
+            int32_t L = (len + p.split - 1) / p.split;
+            if (L < 8) L = len < 8 ? len : 8;
+            const int32_t nchunks = (len + L - 1) / L;
+            g.t0 = g.ut0 + min(c, nchunks) * L;
+            g.t1 = c < nchunks ? min(g.t0 + L, g.ut1) : g.t0;
+            g.skip = c >= nchunks - 1 ? p.split : 0;
+        } else {
+            // fixed key chunks: chunk c's share of the block's tile range
+            if (g.ct0 < g.ct1) {
+                g.t0 = max(g.ct0, g.ut0);
+                g.t1 = min(g.ct1, g.ut1);
+                if (g.t1 < g.t0) g.t1 = g.t0;
+            }
+            const int32_t c_lo = g.ut0 / p.tiles_per_chunk;
+            const int32_t c_hi = (g.ut1 - 1) / p.tiles_per_chunk;
+            g.skip = c < c_lo ? c_lo : (c >= c_hi ? p.split : 0);
         }
     }
     return g;
@@ -517,23 +540,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const int32_t b = p.num_blocks - 1 - int32_t(u / uint32_t(p.split));
                 const int32_t c = int32_t(u % uint32_t(p.split));
-                const Geometry geo = unit_geometry(p, b, c);
-                // The block's chunks that meet its windows are [c_lo, c_hi]; move the shared
-                // counter past the empty ones this claim has revealed, so no CTA spends a
-                // claim on them (a hint: a unit that is claimed anyway is found empty).
-                if (lane == 0) {
-                    const uint32_t base = u - uint32_t(c);
-                    if (geo.ut0 >= geo.ut1) {
-                        atomicMax(&p.sched->next_unit, base + uint32_t(p.split));
-                    } else {
-                        const int32_t c_lo = geo.ut0 / p.tiles_per_chunk;
-                        const int32_t c_hi = (geo.ut1 - 1) / p.tiles_per_chunk;
-                        if (c < c_lo)
-                            atomicMax(&p.sched->next_unit, base + uint32_t(c_lo));
-                        else if (c >= c_hi)
-                            atomicMax(&p.sched->next_unit, base + uint32_t(p.split));
-                    }
-                }
+                const Geometry geo = unit_geometry(p, b, c, true);
+                // Move the shared counter past the chunks of this block that this claim has
+                // shown to be empty, so no CTA spends a claim on them (a hint: a unit that is
+                // claimed anyway is found empty).
+                if (lane == 0 && geo.skip > 0)
+                    atomicMax(&p.sched->next_unit, u - uint32_t(c) + uint32_t(geo.skip));
                 if (geo.t1 > geo.t0) return geo;
             }
         };

@@ -60,11 +60,11 @@ def test_is_supported_truth_table(lib):
 
 
 def test_default_split(lib):
-    # about 4, 8 or 16 units per SM for many, some or few row blocks; chunks of at least
+    # about 4, 20 or 16 units per SM for many, some or few row blocks; chunks of at least
     # 8 key tiles
     assert fm.default_split(8192, 8192, 152) == 1
     assert fm.default_split(16384, 32000, 152) == 1
-    assert fm.default_split(4096, 32768, 152) == 3
+    assert fm.default_split(4096, 32768, 152) == 6
     assert fm.default_split(1024, 131072, 152) == 19
     assert fm.default_split(64, 256, 152) == 1
     assert fm.default_split(1, 1, 152) == 1
