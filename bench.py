@@ -396,7 +396,7 @@ def run_topk(args):
 
 
 # Revision tag of the kernel the committed ncu traffic figure was taken on.
-KERNEL_REV = "v4"
+KERNEL_REV = "v5"
 
 
 def main(argv=None):
