@@ -200,6 +200,7 @@ __device__ __forceinline__ void topk_select_buffer(TopkSmem& s, unsigned long lo
                                                    uint32_t kk)
 {
     const int tid = threadIdx.x;
+    __syncthreads();  // every thread holds its arguments (n may be a count reset below)
     for (int pass = 0; pass < 2; ++pass) {
         const int shift = pass == 0 ? 10 : 0;
         const uint32_t nb = pass == 0 ? 2048u : 1024u;
@@ -469,8 +470,17 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkParams 
             int32_t idx = -1;
             float val = __int_as_float(0xff800000);
             if (j < n_sel) {
-                idx = int32_t(0xFFFFFFFFu - uint32_t(s.cand[j] & 0xFFFFFFFFull));
-                val = x[idx];
+                const unsigned long long cv = s.cand[j];
+                idx = int32_t(0xFFFFFFFFu - uint32_t(cv & 0xFFFFFFFFull));
+                const uint32_t key = uint32_t(cv >> 32);
+                if (key == 0x80000000u) {
+                    // a zero: the key folded its sign away, so read it back (every composite
+                    // carries an index below N; the guard keeps the read in bounds)
+                    val = uint32_t(idx) < uint32_t(N) ? x[idx] : __int_as_float(0x7fc00000);
+                } else {
+                    // the key's inverse: the value itself, with no dependent global read
+                    val = __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
+                }
             }
             oi[j] = idx;
             if (ov) ov[j] = val;

@@ -31,7 +31,11 @@ def _check(x: np.ndarray, k: int, gpu_rows=None, what=""):
 
 @pytest.mark.parametrize("M,N,k", [(1, 1, 1), (3, 5, 8), (64, 300, 1), (64, 300, 7),
                                    (40, 1000, 512), (33, 4097, 512), (16, 5000, 2048),
-                                   (8, 1500, 2048), (200, 2500, 64)])
+                                   (8, 1500, 2048), (200, 2500, 64),
+                                   # many rows: several row groups per CTA, of one, two
+                                   # and four warps, with rows left over for some groups
+                                   (1000, 2000, 100), (1111, 4100, 256), (700, 9000, 512),
+                                   (300, 20000, 1024)])
 def test_random_rows(M, N, k):
     _check(workloads.draw_logits(M, N, seed=M * 7 + k), k, what=f"{M}x{N} k={k}")
 
@@ -96,10 +100,11 @@ def test_indexer_pipeline_top512_matches_the_oracle_pipeline():
     assert same >= 0.9 * len(rows) and overlap >= 500, (same, overlap)
 
 
-def test_crowded_threshold_bin_takes_the_multi_pass_path():
-    # more than 8192 entries share the top 11 key bits of the k-th largest: the select
-    # resolves the remaining bits with further passes over the row
-    N = 20000
+@pytest.mark.parametrize("N", [3000, 20000])
+def test_crowded_threshold_bin_takes_the_multi_pass_path(N):
+    # more entries than the threshold-bin buffer holds (1024 per warp of the row's group,
+    # at most 8192) share the top 11 key bits of the k-th largest: the select resolves the
+    # remaining bits with further passes over the row
     x = np.empty((5, N), dtype=np.float32)
     x[0] = 1.0                                            # all equal: ties in index order
     x[1] = 1.0 + np.arange(N, dtype=np.float32) * 2.0 ** -23   # distinct, one top bin
