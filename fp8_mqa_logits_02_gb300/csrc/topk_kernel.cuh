@@ -12,13 +12,13 @@
 //   1. read the row, histogram the top 11 key bits (a private histogram per warp, so hot
 //      bins do not serialise the whole block);
 //   2. the bin b0 holding the k-th largest is found from the top;
-//   3. read the row again: keys above b0 go straight to the winners, keys in b0 to a
-//      shared-memory buffer, where two more radix passes (key bits 20..10 and 9..0) pick
-//      the rest and equal keys are taken by index;
+//   3. read the row again and append the keys of b0 and above to a shared-memory buffer
+//      (one append per key); those above b0 are winners, and two more radix passes (key
+//      bits 20..10 and 9..0) over those of b0 pick the rest, equal keys taken by index;
 //   4. the winners (at most 2048) are sorted by a bitonic network and written.
-// When b0 holds more entries than the buffer, the remaining 21 key bits are resolved by
-// two more histogram passes over the row and a collect pass that takes the ties in index
-// order.
+// When b0 and the bins above hold more entries than the buffer, the remaining 21 key bits
+// of b0 are resolved by two more histogram passes over the row and a collect pass that
+// takes the ties in index order.
 #pragma once
 
 #include <cstdint>
@@ -45,7 +45,7 @@ struct TopkSmem {
     unsigned long long cand[kTopkMaxK];
     unsigned long long tbuf[kTopkTieCap];
     uint32_t scratch[kTopkWarps];
-    uint32_t sel_bin, sel_above, sel_count, n_cand, n_tie, tie_base;
+    uint32_t sel_bin, sel_above, sel_count, n_cand, n_tie, tie_base, n_spare;
 };
 constexpr uint32_t kTopkSmemBytes = sizeof(TopkSmem);
 static_assert(kTopkSmemBytes <= 232448, "top-k shared memory");
@@ -390,24 +390,37 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkParams 
         const uint32_t total = topk_find_bin(s, s.hist, kTopkBins, uint32_t(k));
         const bool take_all = total <= uint32_t(k);
         const uint32_t b0 = s.sel_bin, above0 = s.sel_above, count0 = s.sel_count;
-        const bool fast = take_all || count0 <= uint32_t(kTopkTieCap);
+        const bool fast = take_all || above0 + count0 <= uint32_t(kTopkTieCap);
 
         if (fast) {
-            // ---- 3. winners above b0, the b0 entries into the buffer
+            // ---- 3. one append per entry: every finite entry when all are winners, else
+            // the entries of b0 and above into the buffer
+            unsigned long long* const spare = reinterpret_cast<unsigned long long*>(&s.whist[0][0]);
+            unsigned long long* const dst = take_all ? s.cand : s.tbuf;
+            uint32_t* const cnt = take_all ? &s.n_cand : &s.n_tie;
             topk_for_row(x, N, [&](int i, float v, bool valid) {
                 const bool in = valid && topk_eligible(v);
                 const uint32_t key = in ? topk_key(v) : 0u;
-                const uint32_t d = key >> 21;
-                const unsigned long long c = topk_composite(key, i);
-                topk_append(s.cand, &s.n_cand, c, in && (take_all || d > b0));
-                topk_append(s.tbuf, &s.n_tie, c, in && !take_all && d == b0);
+                topk_append(dst, cnt, topk_composite(key, i), in && (take_all || (key >> 21) >= b0));
             });
             __syncthreads();
             if (!take_all) {
-                // the kk largest of the b0 entries, ties by index; the per-warp histograms
-                // are free now and hold the spare buffer
-                topk_select_buffer(s, s.tbuf, reinterpret_cast<unsigned long long*>(&s.whist[0][0]),
-                                   s.n_tie, uint32_t(k) - above0);
+                // split the buffer: entries above b0 are winners, those of b0 go to the
+                // spare buffer (the per-warp histograms, free now), where the kk largest of
+                // them are selected with ties by index
+                const uint32_t n = s.n_tie;
+                const uint32_t rounds = (n + kTopkThreads - 1) / kTopkThreads;
+                if (tid == 0) s.n_spare = 0;
+                __syncthreads();
+                for (uint32_t r = 0; r < rounds; ++r) {
+                    const uint32_t j = r * kTopkThreads + tid;
+                    const unsigned long long c = j < n ? s.tbuf[j] : 0ull;
+                    const uint32_t d = uint32_t(c >> 53);
+                    topk_append(s.cand, &s.n_cand, c, j < n && d > b0);
+                    topk_append(spare, &s.n_spare, c, j < n && d == b0);
+                }
+                __syncthreads();
+                topk_select_buffer(s, spare, s.tbuf, s.n_spare, uint32_t(k) - above0);
             }
         } else {
             // ---- 3'. the threshold bin is too large for the buffer: resolve the other 21
