@@ -6,6 +6,7 @@
 #include <cudaTypedefs.h>
 
 #include <atomic>
+#include <algorithm>
 #include <cstdint>
 #include <cstring>
 #include <functional>
@@ -324,17 +325,38 @@ int fp8_mqa_logits_is_supported(int64_t M, int64_t N, int32_t H, int32_t D)
 
 int fp8_mqa_logits_default_split(int64_t M, int64_t N, int32_t num_sms)
 {
-    // Enough units for the dynamic scheduler to balance the tail, and no more: every unit
-    // costs a claim, a Q load and a pipeline restart.  About 4 units per SM when there are
-    // four or more row blocks per SM (heaviest-first order then balances whole blocks), 20
-    // with two to four blocks per SM, and 16 under two (every block is then split into many
-    // chunks of equal work and the last chunks decide the finish).  Chunks keep at least 8
-    // key tiles; the kernel splits a block with narrow windows along its own tile range.
+    // Larger problems (below): enough units for the dynamic scheduler to balance the tail,
+    // and no more, since every unit costs a claim, a Q load and a pipeline restart.  About 4
+    // units per SM when there are four or more row blocks per SM (heaviest-first order then
+    // balances whole blocks), 20 with two to four blocks per SM, and 16 under two (every
+    // block is then split into many chunks of equal work and the last chunks decide the
+    // finish).  Chunks keep at least 8 key tiles; the kernel splits a block with narrow
+    // windows along its own tile range.
     if (M <= 0 || N <= 0) return 1;
     if (num_sms < 1) num_sms = 1;
     const int64_t tiles = (N + fp8mqa::kTileKeys - 1) / fp8mqa::kTileKeys;
     const int64_t blocks = (M + fp8mqa::kRows - 1) / fp8mqa::kRows;
     const int64_t sms = num_sms;
+    if (blocks * tiles <= 64 * sms) {
+        // Small problems (64 key tiles per SM or fewer): launch and set-up dominate, so take
+        // the split with the least estimated time.  Units run in rounds of one per SM, and
+        // a unit costs its tiles plus a fixed set-up of about 3.3 tiles (its claim, Q load
+        // and pipeline fill: about 2 us against about 0.6 us per tile, measured on GB300).
+        constexpr double kUnitSetupTiles = 3.3;
+        const int64_t s_max = std::min<int64_t>(tiles, 4 * sms / blocks + 1);
+        int64_t best = 1;
+        double best_cost = 0;
+        for (int64_t s = 1; s <= s_max; ++s) {
+            const int64_t tpc = (tiles + s - 1) / s;
+            const int64_t units = blocks * ((tiles + tpc - 1) / tpc);
+            const double cost = double((units + sms - 1) / sms) * (kUnitSetupTiles + double(tpc));
+            if (s == 1 || cost < best_cost) {
+                best = s;
+                best_cost = cost;
+            }
+        }
+        return int(best);
+    }
     const int64_t per_sm = blocks < 2 * sms ? 16 : (blocks < 4 * sms ? 20 : 4);
     const int64_t target = per_sm * sms;
     int64_t s = (target + blocks - 1) / blocks;
