@@ -337,8 +337,8 @@ int fp8_mqa_logits_default_split(int64_t M, int64_t N, int32_t num_sms)
     const int64_t tiles = (N + fp8mqa::kTileKeys - 1) / fp8mqa::kTileKeys;
     const int64_t blocks = (M + fp8mqa::kRows - 1) / fp8mqa::kRows;
     const int64_t sms = num_sms;
-    if (blocks * tiles <= 64 * sms) {
-        // Small problems (64 key tiles per SM or fewer): launch and set-up dominate, so take
+    if (blocks * tiles <= 128 * sms) {
+        // Small problems (128 key tiles per SM or fewer): launch and set-up weigh, so take
         // the split with the least estimated time.  Units run in rounds of one per SM, and
         // a unit costs its tiles plus a fixed set-up of about 3.3 tiles (its claim, Q load
         // and pipeline fill: about 2 us against about 0.6 us per tile, measured on GB300).

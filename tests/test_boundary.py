@@ -66,9 +66,8 @@ def test_default_split(lib):
     assert fm.default_split(16384, 32000, 152) == 1
     assert fm.default_split(4096, 32768, 152) == 6
     assert fm.default_split(1024, 131072, 152) == 19
-    assert fm.default_split(128, 131072, 152) == 128
     assert fm.default_split(1, 1, 152) == 1
-    # at 64 key tiles per SM or fewer, the split with the fewest rounds x (set-up + tiles
+    # at 128 key tiles per SM or fewer, the split with the fewest rounds x (set-up + tiles
     # per unit): one round of units where it fits, whole rows where they already fill it
     assert fm.default_split(64, 256, 152) == 2
     assert fm.default_split(64, 8192, 152) == 16     # 128 units of 4 tiles
@@ -76,6 +75,9 @@ def test_default_split(lib):
     assert fm.default_split(128, 32768, 152) == 9    # 144 units of 29 tiles
     assert fm.default_split(2048, 2048, 152) == 1
     assert fm.default_split(1024, 1024, 152) == 1
+    assert fm.default_split(128, 131072, 152) == 19  # 304 units of 54 tiles: two rounds
+    assert fm.default_split(256, 65536, 152) == 9
+    assert fm.default_split(2048, 8192, 152) == 1
     for M in (1, 7, 100, 5000):
         for N in (1, 129, 4000, 100000):
             s = fm.default_split(M, N, 152)
