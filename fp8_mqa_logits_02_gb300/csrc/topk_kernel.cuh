@@ -312,7 +312,7 @@ __device__ __forceinline__ void topk_sort_desc_reg(unsigned long long* buf, int 
                     const unsigned long long o = buf[e ^ stride];
                     const bool desc = (e & size) == 0, lo = (e & stride) == 0;
                     const bool keep_max = desc == lo;
-                    v[j] = keep_max ? (v[j] > o ? v[j] : o) : (v[j] < o ? v[j] : o);
+                    v[j] = (o > v[j]) == keep_max ? o : v[j];  // composites differ, but for padding zeros
                 }
                 __syncthreads();
             } else if (stride >= E) {
@@ -323,7 +323,7 @@ __device__ __forceinline__ void topk_sort_desc_reg(unsigned long long* buf, int 
                     const unsigned long long o = __shfl_xor_sync(0xffffffffu, v[j], lanes);
                     const bool desc = (e & size) == 0, lo = (e & stride) == 0;
                     const bool keep_max = desc == lo;
-                    v[j] = keep_max ? (v[j] > o ? v[j] : o) : (v[j] < o ? v[j] : o);
+                    v[j] = (o > v[j]) == keep_max ? o : v[j];  // composites differ, but for padding zeros
                 }
             } else if (stride == 1) {
                 topk_sort_in_thread<E, 1>(v, tid, size);
