@@ -269,6 +269,8 @@ def run_gpu(args):
     hout = torch.empty((M, N), dtype=torch.float32).pin_memory()
     wsp = torch.empty(fm.host_workspace_bytes(M, N), dtype=torch.uint8, device=dev)
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hkv, hw, hks, hke))
+    if not args.clean:
+        h2d += hout.numel() * 4  # with clean_logits = 0 the logits buffer goes in as well
     d2h = hout.numel() * 4
 
     def e2e_step():

@@ -227,6 +227,47 @@ int launch(const uint8_t* q, const uint8_t* k, const float* kv, const float* w,
 uint64_t align256(uint64_t x) { return (x + 255) & ~uint64_t(255); }
 
 // ---------------------------------------------------------------------------------------
+// Host-buffer entry (fp8_mqa_logits_host): the rows go in chunks, so that the copies in
+// both directions and the kernels overlap.  Inputs travel on one library stream, the
+// chunks' kernels run on the caller's stream, and each chunk's logits go back on a second
+// library stream as soon as its kernel is done.  Events fork the two streams from the
+// caller's stream at the start of a call and join them back at its end.
+constexpr int kHostChunksMax = 8;
+constexpr uint64_t kHostChunkBytes = uint64_t(32) << 20;  // logits per chunk, about
+
+struct HostPipe {
+    std::mutex mu;  // one call enqueues at a time per device
+    bool ready = false;
+    int init_status = FP8MQA_OK;
+    cudaStream_t in = nullptr, out = nullptr;
+    cudaEvent_t start = nullptr, done = nullptr;
+    cudaEvent_t in_ev[kHostChunksMax] = {}, k_ev[kHostChunksMax] = {};
+};
+
+HostPipe g_pipe[kMaxDevices];
+
+// Creates the pipeline's streams and events on first use (under the device's lock); they
+// live until the process exits.
+int host_pipe_init(HostPipe& hp)
+{
+    if (hp.ready) return hp.init_status;
+    hp.ready = true;
+    const unsigned ev_flags = cudaEventDisableTiming;
+    bool ok = cudaStreamCreateWithFlags(&hp.in, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&hp.out, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaEventCreateWithFlags(&hp.start, ev_flags) == cudaSuccess &&
+              cudaEventCreateWithFlags(&hp.done, ev_flags) == cudaSuccess;
+    for (int c = 0; ok && c < kHostChunksMax; ++c)
+        ok = cudaEventCreateWithFlags(&hp.in_ev[c], ev_flags) == cudaSuccess &&
+             cudaEventCreateWithFlags(&hp.k_ev[c], ev_flags) == cudaSuccess;
+    if (!ok) {
+        cudaGetLastError();
+        hp.init_status = FP8MQA_ERR_CUDA;
+    }
+    return hp.init_status;
+}
+
+// ---------------------------------------------------------------------------------------
 // Allocation-free variant (fp8_mqa_logits_noalloc).  Its scratch -- the scheduler's work
 // counters and a status word -- lives in the file-scope array below instead of memory
 // from cudaMalloc.  Host code may not pass the array's name to a kernel (on the host it
@@ -431,20 +472,57 @@ int fp8_mqa_logits_host(const uint8_t* q_fp8, const uint8_t* k_fp8, const float*
     int32_t* dke = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(dks) + align256(m * 4));
     float* dout = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(dke) + align256(m * 4));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const cudaMemcpyKind h2d = cudaMemcpyHostToDevice;
-    if (cudaMemcpyAsync(dq, q_fp8, m * H * D, h2d, s) != cudaSuccess ||
-        cudaMemcpyAsync(dk, k_fp8, n * D, h2d, s) != cudaSuccess ||
-        cudaMemcpyAsync(dkv, kv_scale, n * 4, h2d, s) != cudaSuccess ||
-        cudaMemcpyAsync(dw, w, m * H * 4, h2d, s) != cudaSuccess ||
-        cudaMemcpyAsync(dks, ks, m * 4, h2d, s) != cudaSuccess ||
-        cudaMemcpyAsync(dke, ke, m * 4, h2d, s) != cudaSuccess)
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= fp8mqa::kMaxDevices) {
+        cudaGetLastError();
         return FP8MQA_ERR_CUDA;
-    if (!clean_logits && cudaMemcpyAsync(dout, out, m * n * 4, h2d, s) != cudaSuccess)
-        return FP8MQA_ERR_CUDA;
-    rc = fp8mqa::launch(dq, dk, dkv, dw, dks, dke, dout, M, N, clean_logits, split_n, s);
+    }
+    int err = FP8MQA_OK;
+    if (!fp8mqa::device_state(&err)) return err;
+    fp8mqa::HostPipe& hp = fp8mqa::g_pipe[dev];
+    std::lock_guard<std::mutex> lock(hp.mu);
+    rc = fp8mqa::host_pipe_init(hp);
     if (rc != FP8MQA_OK) return rc;
-    if (cudaMemcpyAsync(out, dout, m * n * 4, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+
+    // chunks of whole 8-row blocks, about kHostChunkBytes of logits each
+    int64_t chunks = int64_t((m * n * 4) / fp8mqa::kHostChunkBytes);
+    chunks = std::max<int64_t>(1, std::min<int64_t>(chunks, fp8mqa::kHostChunksMax));
+    int64_t rows = (M + chunks - 1) / chunks;
+    rows = (rows + fp8mqa::kRows - 1) / fp8mqa::kRows * fp8mqa::kRows;
+    chunks = (M + rows - 1) / rows;
+
+    const cudaMemcpyKind h2d = cudaMemcpyHostToDevice, d2h = cudaMemcpyDeviceToHost;
+    bool ok = cudaEventRecord(hp.start, s) == cudaSuccess &&
+              cudaStreamWaitEvent(hp.in, hp.start, 0) == cudaSuccess &&
+              cudaStreamWaitEvent(hp.out, hp.start, 0) == cudaSuccess &&
+              cudaMemcpyAsync(dk, k_fp8, n * D, h2d, hp.in) == cudaSuccess &&
+              cudaMemcpyAsync(dkv, kv_scale, n * 4, h2d, hp.in) == cudaSuccess;
+    for (int64_t c = 0; ok && c < chunks; ++c) {
+        const uint64_t r0 = uint64_t(c * rows), mr = uint64_t(std::min<int64_t>(rows, M - c * rows));
+        ok = cudaMemcpyAsync(dq + r0 * H * D, q_fp8 + r0 * H * D, mr * H * D, h2d, hp.in) == cudaSuccess &&
+             cudaMemcpyAsync(dw + r0 * H, w + r0 * H, mr * H * 4, h2d, hp.in) == cudaSuccess &&
+             cudaMemcpyAsync(dks + r0, ks + r0, mr * 4, h2d, hp.in) == cudaSuccess &&
+             cudaMemcpyAsync(dke + r0, ke + r0, mr * 4, h2d, hp.in) == cudaSuccess &&
+             (clean_logits ||
+              cudaMemcpyAsync(dout + r0 * n, out + r0 * n, mr * n * 4, h2d, hp.in) == cudaSuccess) &&
+             cudaEventRecord(hp.in_ev[c], hp.in) == cudaSuccess &&
+             cudaStreamWaitEvent(s, hp.in_ev[c], 0) == cudaSuccess;
+        if (!ok) break;
+        rc = fp8mqa::launch(dq + r0 * H * D, dk, dkv, dw + r0 * H, dks + r0, dke + r0, dout + r0 * n,
+                            int64_t(mr), N, clean_logits, split_n, s);
+        if (rc != FP8MQA_OK) break;
+        ok = cudaEventRecord(hp.k_ev[c], s) == cudaSuccess &&
+             cudaStreamWaitEvent(hp.out, hp.k_ev[c], 0) == cudaSuccess &&
+             cudaMemcpyAsync(out + r0 * n, dout + r0 * n, mr * n * 4, d2h, hp.out) == cudaSuccess;
+    }
+    // join: later work on the caller's stream sees every copy of this call
+    const bool joined = cudaEventRecord(hp.done, hp.out) == cudaSuccess &&
+                        cudaStreamWaitEvent(s, hp.done, 0) == cudaSuccess;
+    if (rc != FP8MQA_OK) return rc;
+    if (!ok || !joined) {
+        cudaGetLastError();
         return FP8MQA_ERR_CUDA;
+    }
     return FP8MQA_OK;
 }
 

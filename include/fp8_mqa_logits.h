@@ -116,13 +116,21 @@ FP8MQA_API int fp8_mqa_logits_check_error(void* stream);
 FP8MQA_API uint64_t fp8_mqa_logits_host_workspace_bytes(int64_t M, int64_t N, int32_t H, int32_t D);
 
 /*
- * fp8_mqa_logits_host -- the same operation on HOST buffers.  Enqueues on `stream`:
- * host->device copies of q, k, kv_scale, w, ks, ke into `workspace`, the kernel, and a
- * device->host copy of all of out.  Host buffers should be pinned (cudaHostAlloc) for
- * the copies to be asynchronous; pageable memory works but the copies then block.
- * The call returns after enqueueing; synchronize `stream` before reading `out`.
- * With clean_logits = 0, the device copy of out is first filled from the host `out`, so
- * untouched entries come back unchanged.
+ * fp8_mqa_logits_host -- the same operation on HOST buffers.  Enqueues host->device
+ * copies of q, k, kv_scale, w, ks, ke into `workspace`, the kernel, and device->host
+ * copies of all of out, ordered after the work already on `stream`; work enqueued on
+ * `stream` after the call runs after all of it.  The rows go in chunks of about 32 MB of
+ * logits (at most 8): the inputs travel on a library stream, the chunks' kernels run on
+ * `stream`, and each chunk's logits go back on a second library stream as soon as its
+ * kernel is done, so the copies in both directions and the kernels overlap.  The two
+ * library streams and their events are created on a device's first call and live until
+ * the process exits; calls on one device enqueue one at a time, and their copies share
+ * the library streams.  The call can be captured into a CUDA graph (the library streams
+ * fork from `stream` by an event and join it again).  Host buffers should be pinned
+ * (cudaHostAlloc) for the copies to be asynchronous; pageable memory works but the
+ * copies then block.  The call returns after enqueueing; synchronize `stream` before
+ * reading `out`.  With clean_logits = 0, the device copy of out is first filled from the
+ * host `out`, so untouched entries come back unchanged.
  *   workspace        device pointer, 256-byte aligned, at least
  *                    fp8_mqa_logits_host_workspace_bytes(M, N, H, D) bytes, caller-owned.
  *   workspace_bytes  its size.

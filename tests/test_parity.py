@@ -158,6 +158,33 @@ def test_host_buffer_entry_point():
     assert_parity(out.numpy(), ref, window_mask(inp["ks"], inp["ke"], 900), True, what="host")
 
 
+@pytest.mark.parametrize("clean", [True, False])
+def test_host_buffer_entry_point_in_chunks(clean):
+    # 4096 x 8192 logits are 134 MB: the host entry splits them into four row chunks whose
+    # input copies, kernels and read-backs overlap.  Parity on sampled rows of every chunk;
+    # with clean_logits = 0 the poisoned host buffer must come back untouched outside the
+    # windows.  The result also equals the device-buffer entry's, bit for bit (the kernel
+    # output does not depend on how rows or keys are split).
+    M, N = 4096, 8192
+    inp = _inputs(M, N, "causal", seed=17)
+    cpu = {k: torch.from_numpy(inp[k]).pin_memory()
+           for k in ("q", "k", "kv_scale", "w", "ks", "ke")}
+    out = poisoned(M, N, device="cpu").pin_memory()
+    ws = torch.empty(fm.host_workspace_bytes(M, N), dtype=torch.uint8, device="cuda")
+    fm.fp8_mqa_logits_host(cpu["q"], cpu["k"], cpu["kv_scale"], cpu["w"], cpu["ks"], cpu["ke"],
+                           out, ws, clean_logits=clean)
+    torch.cuda.synchronize()
+    assert fm.check_error() == 0
+    host = out.numpy()
+    rows = np.array(sorted({0, 1, 1023, 1024, 1025, 2047, 2048, 3071, 3072, 4094, 4095}
+                           | set(np.random.default_rng(3).choice(M, 21, replace=False).tolist())))
+    ref = run_oracle(inp, clean=clean, rows=rows)
+    assert_parity(host[rows], ref, window_mask(inp["ks"], inp["ke"], N, rows), clean,
+                  what=f"host chunks clean={clean}")
+    dev = run_gpu(inp, clean=clean)
+    assert np.array_equal(host.view(np.uint32), dev.view(np.uint32))
+
+
 # ------------------------------------------------------------------ full-size workloads
 def _sample_rows(M, nrand, seed):
     rng = np.random.default_rng(seed)
