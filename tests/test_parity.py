@@ -254,6 +254,35 @@ def test_call_captured_in_a_cuda_graph():
         assert_parity(out.cpu().numpy(), ref, inside, True, what="graph replay")
 
 
+def test_host_entry_captured_in_a_cuda_graph():
+    # The host-buffer entry forks its two library streams from the caller's stream and joins
+    # them again, so a call (here in two row chunks: 67 MB of logits) can be captured and
+    # replayed; each replay copies in, computes and copies back the whole output.
+    M, N = 2048, 8192
+    inp = _inputs(M, N, "causal", seed=19)
+    cpu = {k: torch.from_numpy(inp[k]).pin_memory()
+           for k in ("q", "k", "kv_scale", "w", "ks", "ke")}
+    out = poisoned(M, N, device="cpu").pin_memory()
+    ws = torch.empty(fm.host_workspace_bytes(M, N), dtype=torch.uint8, device="cuda")
+    args = (cpu["q"], cpu["k"], cpu["kv_scale"], cpu["w"], cpu["ks"], cpu["ke"], out, ws)
+    fm.fp8_mqa_logits_host(*args)  # the first call on the device sets the library up
+    torch.cuda.synchronize()
+    rows = np.array(sorted({0, 7, 1023, 1024, 1031, 2047}
+                           | set(np.random.default_rng(5).choice(M, 10, replace=False).tolist())))
+    ref = run_oracle(inp, clean=True, rows=rows)
+    inside = window_mask(inp["ks"], inp["ke"], N, rows)
+    s = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        fm.fp8_mqa_logits_host(*args, stream=s)
+    for _ in range(2):
+        out.copy_(poisoned(M, N, device="cpu"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert fm.check_error() == 0
+        assert_parity(out.numpy()[rows], ref, inside, True, what="host entry graph replay")
+
+
 # ------------------------------------------------------------------ randomized configurations
 def _random_config(rng):
     M = int(rng.integers(1, 100))
