@@ -423,8 +423,8 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkParams 
                 topk_select_buffer(s, spare, s.tbuf, s.n_spare, uint32_t(k) - above0);
             }
         } else {
-            // ---- 3'. the threshold bin is too large for the buffer: resolve the other 21
-            // key bits with two more histogram passes (10 and 11 bits)
+            // ---- 3'. b0 and the bins above hold more entries than the buffer: resolve the
+            // other 21 key bits of b0 with two more histogram passes (11 and 10 bits)
             uint32_t prefix = b0 << 21, pmask = 0x7FFu << 21;
             uint32_t kk = uint32_t(k) - above0;
             uint32_t tie_total = count0;
