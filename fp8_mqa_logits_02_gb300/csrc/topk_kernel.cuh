@@ -7,8 +7,10 @@
 // selected), ordered by value descending and, for equal values, by index ascending (-0.0
 // equals +0.0); slots past the row's finite entries get index -1 and value -inf.
 //
-// One CTA per row at a time (persistent grid of one CTA per SM, so a row's second read
-// comes from L2).  Radix select on an order-preserving 32-bit key:
+// A persistent grid of at most one CTA per SM walks the rows (a row's second read comes from
+// L2): rows of up to 32768 keys with k <= 512 two at a time, 256 threads each on a named
+// barrier of their own, so one row's barrier waits overlap the other's work; other rows one
+// at a time with all 512 threads.  Radix select on an order-preserving 32-bit key:
 //   1. read the row, histogram the top 11 key bits (a private histogram per warp, so hot
 //      bins do not serialise the whole block);
 //   2. the bin b0 holding the k-th largest is found from the top;
@@ -25,11 +27,9 @@
 
 namespace fp8mqa {
 
-constexpr int kTopkThreads = 512;
-constexpr int kTopkWarps = kTopkThreads / 32;
+constexpr int kTopkThreads = 512;  // threads per CTA
 constexpr int kTopkMaxK = 2048;
 constexpr int kTopkBins = 2048;      // 11-bit digits
-constexpr int kTopkTieCap = 8192;    // entries of the threshold bin sorted in shared memory
 
 struct TopkParams {
     const float* logits;
@@ -39,16 +39,49 @@ struct TopkParams {
     float* values;     // [M, k] or null
 };
 
+// A CTA works on kTopkThreads / NT rows at once, NT threads each, a row's threads
+// synchronising on a named barrier of their own (the whole CTA's barrier when NT is the
+// CTA).  One row's shared memory; TIE entries of the threshold bin (and the bins above it)
+// are selected in it.
+template <int NT, int TIE>
 struct TopkSmem {
-    uint32_t whist[kTopkWarps][kTopkBins];
+    static constexpr int kNT = NT;
+    static constexpr int kTie = TIE;
+    uint32_t whist[NT / 32][kTopkBins];  // per-warp histograms, later the spare buffer
     uint32_t hist[kTopkBins];
     unsigned long long cand[kTopkMaxK];
-    unsigned long long tbuf[kTopkTieCap];
-    uint32_t scratch[kTopkWarps];
-    uint32_t sel_bin, sel_above, sel_count, n_cand, n_tie, tie_base, n_spare;
+    unsigned long long tbuf[TIE];
+    uint32_t scratch[NT / 32];
+    uint32_t sel_bin, sel_above, sel_count, n_cand, n_tie, tie_base, n_spare, pad;
 };
-constexpr uint32_t kTopkSmemBytes = sizeof(TopkSmem);
+// Rows of up to 32768 keys with k <= 512: two rows per CTA, 256 threads each.  Otherwise one
+// row per CTA with the larger threshold-bin buffer that long rows and k = 2048 need.
+using TopkSmemPair = TopkSmem<256, 2048>;
+using TopkSmemOne = TopkSmem<512, 8192>;
+constexpr uint32_t kTopkSmemBytes = sizeof(TopkSmemOne) > 2 * sizeof(TopkSmemPair)
+                                        ? uint32_t(sizeof(TopkSmemOne))
+                                        : uint32_t(2 * sizeof(TopkSmemPair));
 static_assert(kTopkSmemBytes <= 232448, "top-k shared memory");
+static_assert(sizeof(TopkSmemPair) % 16 == 0, "row slices stay 16-byte aligned");
+static_assert(TopkSmemPair::kTie <= TopkSmemPair::kNT / 32 * kTopkBins / 2 &&
+                  TopkSmemOne::kTie <= TopkSmemOne::kNT / 32 * kTopkBins / 2,
+              "the spare buffer holds the threshold-bin buffer");
+
+// This thread's index among its row's NT threads, and the row's barrier.
+template <int NT>
+__device__ __forceinline__ int topk_tid()
+{
+    return NT == kTopkThreads ? int(threadIdx.x) : int(threadIdx.x) % NT;
+}
+
+template <int NT>
+__device__ __forceinline__ void topk_sync()
+{
+    if constexpr (NT == kTopkThreads)
+        __syncthreads();
+    else
+        asm volatile("bar.sync %0, %1;" ::"r"(1 + int(threadIdx.x) / NT), "n"(NT) : "memory");
+}
 
 // Order-preserving key of a finite float (larger value, larger key; -0.0 and +0.0 equal).
 __device__ __forceinline__ uint32_t topk_key(float x)
@@ -69,45 +102,46 @@ __device__ __forceinline__ unsigned long long topk_composite(uint32_t key, int i
     return (static_cast<unsigned long long>(key) << 32) | (0xFFFFFFFFu - uint32_t(i));
 }
 
-// Block-wide inclusive sum over threads in index order; `scratch` holds kTopkWarps words.
+// Inclusive sum over a row's NT threads in index order; `scratch` holds NT / 32 words.
+template <int NT>
 __device__ __forceinline__ uint32_t topk_block_scan(uint32_t v, uint32_t* scratch, uint32_t& total)
 {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31, warp = topk_tid<NT>() >> 5;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
         const uint32_t o = __shfl_up_sync(0xffffffffu, v, off);
         if (lane >= off) v += o;
     }
     if (lane == 31) scratch[warp] = v;
-    __syncthreads();
+    topk_sync<NT>();
     uint32_t before = 0;
     total = 0;
 #pragma unroll
-    for (int w = 0; w < kTopkWarps; ++w) {
+    for (int w = 0; w < NT / 32; ++w) {
         const uint32_t s = scratch[w];
         if (w < warp) before += s;
         total += s;
     }
-    __syncthreads();
+    topk_sync<NT>();
     return v + before;
 }
 
-// Visit every element of the row once, in chunks whose trip count is uniform over the block
-// (so warp votes inside `fn` see every lane): fn(index, value, valid).  16-byte aligned rows
-// are read four floats per thread per chunk unless kInOrder asks for one element per thread
-// per call, so that successive calls cover the row in index order.
-template <bool kInOrder = false, typename Fn>
+// Visit every element of the row once, in chunks whose trip count is uniform over the row's
+// threads (so warp votes inside `fn` see every lane): fn(index, value, valid).  16-byte
+// aligned rows are read four floats per thread per chunk unless kInOrder asks for one
+// element per thread per call, so that successive calls cover the row in index order.
+template <int NT, bool kInOrder = false, typename Fn>
 __device__ __forceinline__ void topk_for_row(const float* x, int N, Fn&& fn)
 {
-    const int tid = threadIdx.x;
+    const int tid = topk_tid<NT>();
     if (!kInOrder && (reinterpret_cast<uintptr_t>(x) & 15u) == 0) {
         // four 16-byte loads in flight per thread before any is used
         constexpr int kU = 4;
-        for (int c0 = 0; c0 < N; c0 += 4 * kU * kTopkThreads) {
+        for (int c0 = 0; c0 < N; c0 += 4 * kU * NT) {
             float4 v[kU];
 #pragma unroll
             for (int u = 0; u < kU; ++u) {
-                const int i = c0 + 4 * (u * kTopkThreads + tid);
+                const int i = c0 + 4 * (u * NT + tid);
                 v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
                 if (i + 3 < N) {
                     v[u] = __ldg(reinterpret_cast<const float4*>(x + i));
@@ -119,7 +153,7 @@ __device__ __forceinline__ void topk_for_row(const float* x, int N, Fn&& fn)
             }
 #pragma unroll
             for (int u = 0; u < kU; ++u) {
-                const int i = c0 + 4 * (u * kTopkThreads + tid);
+                const int i = c0 + 4 * (u * NT + tid);
                 fn(i, v[u].x, i < N);
                 fn(i + 1, v[u].y, i + 1 < N);
                 fn(i + 2, v[u].z, i + 2 < N);
@@ -127,7 +161,7 @@ __device__ __forceinline__ void topk_for_row(const float* x, int N, Fn&& fn)
             }
         }
     } else {
-        for (int c0 = 0; c0 < N; c0 += kTopkThreads) {
+        for (int c0 = 0; c0 < N; c0 += NT) {
             const int i = c0 + tid;
             fn(i, i < N ? __ldg(x + i) : 0.f, i < N);
         }
@@ -156,16 +190,18 @@ __device__ __forceinline__ void topk_append(unsigned long long* buf, uint32_t* c
 
 // The bin holding the kk-th largest entry, scanning hist[0, nb) from the top; writes
 // sel_bin, sel_above (entries in higher bins) and sel_count (entries in the bin).  Returns
-// the total count.  Uniform over the block.
-__device__ __forceinline__ uint32_t topk_find_bin(TopkSmem& s, const uint32_t* hist, uint32_t nb,
+// the total count.  Uniform over the row's threads.
+template <typename S>
+__device__ __forceinline__ uint32_t topk_find_bin(S& s, const uint32_t* hist, uint32_t nb,
                                                   uint32_t kk)
 {
-    const int tid = threadIdx.x;
-    const int per = int(nb) / kTopkThreads;
+    constexpr int NT = S::kNT;
+    const int tid = topk_tid<NT>();
+    const int per = int(nb) / NT;
     uint32_t run = 0;
     for (int j = 0; j < per; ++j) run += hist[nb - 1 - (tid * per + j)];
     uint32_t total = 0;
-    const uint32_t incl = topk_block_scan(run, s.scratch, total);
+    const uint32_t incl = topk_block_scan<NT>(run, s.scratch, total);
     const uint32_t excl = incl - run;
     if (kk <= total && excl < kk && incl >= kk) {
         uint32_t above = excl;
@@ -181,13 +217,12 @@ __device__ __forceinline__ uint32_t topk_find_bin(TopkSmem& s, const uint32_t* h
             above += h;
         }
     }
-    __syncthreads();
+    topk_sync<NT>();
     return total;
 }
 
-// Bitonic sort of buf[0, n) descending (padding with zeros up to a power of two <= cap).
-__device__ __forceinline__ void topk_sort_desc(unsigned long long* buf, int n);
 // Descending sort of buf[0, n), fastest network for n.
+template <int NT>
 __device__ __forceinline__ void topk_sort_any(unsigned long long* buf, int n);
 
 // Move the kk largest composites of buf[0, n) (all with the same top 11 key bits) to the
@@ -195,62 +230,66 @@ __device__ __forceinline__ void topk_sort_any(unsigned long long* buf, int n);
 // entries whose key equals the kk-th largest key; of those, the ones with the lowest index
 // are taken (a sort of just these ties when the cut falls inside them).  `spare` holds at
 // least n composites.
-__device__ __forceinline__ void topk_select_buffer(TopkSmem& s, unsigned long long* buf,
+template <typename S>
+__device__ __forceinline__ void topk_select_buffer(S& s, unsigned long long* buf,
                                                    unsigned long long* spare, uint32_t n,
                                                    uint32_t kk)
 {
-    const int tid = threadIdx.x;
-    __syncthreads();  // every thread holds its arguments (n may be a count reset below)
+    constexpr int NT = S::kNT;
+    const int tid = topk_tid<NT>();
+    topk_sync<NT>();  // every thread holds its arguments (n may be a count reset below)
     for (int pass = 0; pass < 2; ++pass) {
         const int shift = pass == 0 ? 10 : 0;
         const uint32_t nb = pass == 0 ? 2048u : 1024u;
-        for (uint32_t b = tid; b < nb; b += kTopkThreads) s.hist[b] = 0;
+        for (uint32_t b = tid; b < nb; b += NT) s.hist[b] = 0;
         if (tid == 0) s.n_tie = 0;
-        __syncthreads();
-        for (uint32_t j = tid; j < n; j += kTopkThreads)
+        topk_sync<NT>();
+        for (uint32_t j = tid; j < n; j += NT)
             atomicAdd(&s.hist[uint32_t(buf[j] >> (32 + shift)) & (nb - 1)], 1u);
-        __syncthreads();
+        topk_sync<NT>();
         topk_find_bin(s, s.hist, nb, kk);
         const uint32_t b = s.sel_bin;
         kk -= s.sel_above;
         // entries above the bin are winners; the bin's entries move on to the next pass
-        const uint32_t rounds = (n + kTopkThreads - 1) / kTopkThreads;
+        const uint32_t rounds = (n + NT - 1) / NT;
         for (uint32_t r = 0; r < rounds; ++r) {
-            const uint32_t j = r * kTopkThreads + tid;
+            const uint32_t j = r * NT + tid;
             const unsigned long long c = j < n ? buf[j] : 0ull;
             const uint32_t d = uint32_t(c >> (32 + shift)) & (nb - 1);
             topk_append(s.cand, &s.n_cand, c, j < n && d > b);
             topk_append(spare, &s.n_tie, c, j < n && d == b);
         }
-        __syncthreads();
+        topk_sync<NT>();
         n = s.n_tie;
         unsigned long long* t = buf;
         buf = spare;
         spare = t;
-        __syncthreads();  // every thread has read n before the next pass resets the count
+        topk_sync<NT>();  // every thread has read n before the next pass resets the count
     }
     // buf[0, n) now holds the entries equal to the kk-th largest key; take kk by index
-    if (kk < n) topk_sort_any(buf, int(n));
-    for (uint32_t j = tid; j < kk; j += kTopkThreads) {
+    if (kk < n) topk_sort_any<NT>(buf, int(n));
+    for (uint32_t j = tid; j < kk; j += NT) {
         // the composite orders equal keys by index, so after the sort these are the lowest
         s.cand[s.n_cand + j] = buf[j];
     }
-    __syncthreads();
+    topk_sync<NT>();
     if (tid == 0) s.n_cand += kk;
-    __syncthreads();
+    topk_sync<NT>();
 }
 
-// Bitonic sort of buf[0, n) descending (padding with zeros up to a power of two <= cap).
+// Bitonic sort of buf[0, n) descending (padding with zeros up to the next power of two,
+// which the buffer must hold).
+template <int NT>
 __device__ __forceinline__ void topk_sort_desc(unsigned long long* buf, int n)
 {
-    const int tid = threadIdx.x;
+    const int tid = topk_tid<NT>();
     int P = 1;
     while (P < n) P <<= 1;
-    for (int i = n + tid; i < P; i += kTopkThreads) buf[i] = 0ull;
-    __syncthreads();
+    for (int i = n + tid; i < P; i += NT) buf[i] = 0ull;
+    topk_sync<NT>();
     for (int size = 2; size <= P; size <<= 1) {
         for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            for (int t = tid; t < P / 2; t += kTopkThreads) {
+            for (int t = tid; t < P / 2; t += NT) {
                 const int lo = (t / stride) * stride * 2 + (t % stride);
                 const int hi = lo + stride;
                 const bool desc = (lo & size) == 0;
@@ -260,7 +299,7 @@ __device__ __forceinline__ void topk_sort_desc(unsigned long long* buf, int n)
                     buf[hi] = a;
                 }
             }
-            __syncthreads();
+            topk_sync<NT>();
         }
     }
 }
@@ -284,28 +323,28 @@ __device__ __forceinline__ void topk_sort_in_thread(unsigned long long (&v)[E], 
     }
 }
 
-// Bitonic sort of buf[0, n) descending for n <= 512 * E, with thread t holding elements
+// Bitonic sort of buf[0, n) descending for n <= NT * E, with thread t holding elements
 // t*E .. t*E+E-1 in registers: compare-exchanges at strides below E stay in the thread, at
 // strides below 32*E use warp shuffles, and only the wider ones go through shared memory
-// (two barriers each).
-template <int E>
+// (two barriers each; the buffer holds NT * E entries).
+template <int NT, int E>
 __device__ __forceinline__ void topk_sort_desc_reg(unsigned long long* buf, int n)
 {
-    constexpr int P = kTopkThreads * E;
-    const int tid = threadIdx.x;
+    constexpr int P = NT * E;
+    const int tid = topk_tid<NT>();
     unsigned long long v[E];
 #pragma unroll
     for (int j = 0; j < E; ++j) {
         const int e = tid * E + j;
         v[j] = e < n ? buf[e] : 0ull;
     }
-    __syncthreads();
+    topk_sync<NT>();
     for (int size = 2; size <= P; size <<= 1) {
         for (int stride = size >> 1; stride > 0; stride >>= 1) {
             if (stride >= 32 * E) {
 #pragma unroll
                 for (int j = 0; j < E; ++j) buf[tid * E + j] = v[j];
-                __syncthreads();
+                topk_sync<NT>();
 #pragma unroll
                 for (int j = 0; j < E; ++j) {
                     const int e = tid * E + j;
@@ -314,7 +353,7 @@ __device__ __forceinline__ void topk_sort_desc_reg(unsigned long long* buf, int 
                     const bool keep_max = desc == lo;
                     v[j] = (o > v[j]) == keep_max ? o : v[j];  // composites differ, but for padding zeros
                 }
-                __syncthreads();
+                topk_sync<NT>();
             } else if (stride >= E) {
                 const int lanes = stride / E;
 #pragma unroll
@@ -327,8 +366,10 @@ __device__ __forceinline__ void topk_sort_desc_reg(unsigned long long* buf, int 
                 }
             } else if (stride == 1) {
                 topk_sort_in_thread<E, 1>(v, tid, size);
-            } else {
+            } else if (stride == 2) {
                 topk_sort_in_thread<E, 2>(v, tid, size);
+            } else {
+                topk_sort_in_thread<E, 4>(v, tid, size);
             }
         }
     }
@@ -337,46 +378,59 @@ __device__ __forceinline__ void topk_sort_desc_reg(unsigned long long* buf, int 
         const int e = tid * E + j;
         if (e < n) buf[e] = v[j];
     }
-    __syncthreads();
+    topk_sync<NT>();
 }
 
 // Descending sort of buf[0, n): in registers up to 2048 entries, else in shared memory.
+template <int NT>
 __device__ __forceinline__ void topk_sort_any(unsigned long long* buf, int n)
 {
-    if (n <= kTopkThreads)
-        topk_sort_desc_reg<1>(buf, n);
-    else if (n <= 2 * kTopkThreads)
-        topk_sort_desc_reg<2>(buf, n);
-    else if (n <= 4 * kTopkThreads)
-        topk_sort_desc_reg<4>(buf, n);
-    else
-        topk_sort_desc(buf, n);
+    if (n <= NT)
+        topk_sort_desc_reg<NT, 1>(buf, n);
+    else if (n <= 2 * NT)
+        topk_sort_desc_reg<NT, 2>(buf, n);
+    else if (n <= 4 * NT)
+        topk_sort_desc_reg<NT, 4>(buf, n);
+    else if constexpr (NT * 8 <= kTopkMaxK) {
+        // a row of fewer threads holds up to eight entries each (its buffers hold 2048)
+        if (n <= 8 * NT)
+            topk_sort_desc_reg<NT, 8>(buf, n);
+        else
+            topk_sort_desc<NT>(buf, n);
+    } else {
+        topk_sort_desc<NT>(buf, n);
+    }
 }
 
+template <typename S>
 __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkParams p)
 {
+    constexpr int NT = S::kNT;
+    constexpr int kRowsPerCta = kTopkThreads / NT;
     extern __shared__ __align__(16) uint8_t topk_smem_raw[];
-    TopkSmem& s = *reinterpret_cast<TopkSmem*>(topk_smem_raw);
-    const int tid = threadIdx.x, warp = tid >> 5;
+    const int slot = int(threadIdx.x) / NT;  // which of the CTA's rows this thread works on
+    S& s = reinterpret_cast<S*>(topk_smem_raw)[slot];
+    const int tid = topk_tid<NT>(), warp = tid >> 5;
     const int N = int(p.N);
     const int k = p.k;
     uint32_t* const my_hist = s.whist[warp];
 
-    for (int64_t row = blockIdx.x; row < p.M; row += gridDim.x) {
+    for (int64_t row = int64_t(blockIdx.x) * kRowsPerCta + slot; row < p.M;
+         row += int64_t(gridDim.x) * kRowsPerCta) {
         const float* x = p.logits + row * p.ld;
 
         // ---- 1. top 11 key bits, one histogram per warp, then their sum
         for (int b = tid & 31; b < kTopkBins; b += 32) my_hist[b] = 0;
         __syncwarp();
-        topk_for_row(x, N, [&](int, float v, bool valid) {
+        topk_for_row<NT>(x, N, [&](int, float v, bool valid) {
             const bool in = valid && topk_eligible(v);
             topk_hist_add(my_hist, in ? (topk_key(v) >> 21) : 0u, in);
         });
-        __syncthreads();
-        for (int b = tid; b < kTopkBins; b += kTopkThreads) {
+        topk_sync<NT>();
+        for (int b = tid; b < kTopkBins; b += NT) {
             uint32_t h = 0;
 #pragma unroll
-            for (int w = 0; w < kTopkWarps; ++w) h += s.whist[w][b];
+            for (int w = 0; w < NT / 32; ++w) h += s.whist[w][b];
             s.hist[b] = h;
         }
         if (tid == 0) {
@@ -384,13 +438,13 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkParams 
             s.n_tie = 0;
             s.tie_base = 0;
         }
-        __syncthreads();
+        topk_sync<NT>();
 
         // ---- 2. the bin of the k-th largest
         const uint32_t total = topk_find_bin(s, s.hist, kTopkBins, uint32_t(k));
         const bool take_all = total <= uint32_t(k);
         const uint32_t b0 = s.sel_bin, above0 = s.sel_above, count0 = s.sel_count;
-        const bool fast = take_all || above0 + count0 <= uint32_t(kTopkTieCap);
+        const bool fast = take_all || above0 + count0 <= uint32_t(S::kTie);
 
         if (fast) {
             // ---- 3. one append per entry: every finite entry when all are winners, else
@@ -398,28 +452,28 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkParams 
             unsigned long long* const spare = reinterpret_cast<unsigned long long*>(&s.whist[0][0]);
             unsigned long long* const dst = take_all ? s.cand : s.tbuf;
             uint32_t* const cnt = take_all ? &s.n_cand : &s.n_tie;
-            topk_for_row(x, N, [&](int i, float v, bool valid) {
+            topk_for_row<NT>(x, N, [&](int i, float v, bool valid) {
                 const bool in = valid && topk_eligible(v);
                 const uint32_t key = in ? topk_key(v) : 0u;
                 topk_append(dst, cnt, topk_composite(key, i), in && (take_all || (key >> 21) >= b0));
             });
-            __syncthreads();
+            topk_sync<NT>();
             if (!take_all) {
                 // split the buffer: entries above b0 are winners, those of b0 go to the
                 // spare buffer (the per-warp histograms, free now), where the kk largest of
                 // them are selected with ties by index
                 const uint32_t n = s.n_tie;
-                const uint32_t rounds = (n + kTopkThreads - 1) / kTopkThreads;
+                const uint32_t rounds = (n + NT - 1) / NT;
                 if (tid == 0) s.n_spare = 0;
-                __syncthreads();
+                topk_sync<NT>();
                 for (uint32_t r = 0; r < rounds; ++r) {
-                    const uint32_t j = r * kTopkThreads + tid;
+                    const uint32_t j = r * NT + tid;
                     const unsigned long long c = j < n ? s.tbuf[j] : 0ull;
                     const uint32_t d = uint32_t(c >> 53);
                     topk_append(s.cand, &s.n_cand, c, j < n && d > b0);
                     topk_append(spare, &s.n_spare, c, j < n && d == b0);
                 }
-                __syncthreads();
+                topk_sync<NT>();
                 topk_select_buffer(s, spare, s.tbuf, s.n_spare, uint32_t(k) - above0);
             }
         } else {
@@ -431,21 +485,21 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkParams 
             for (int pass = 1; pass < 3; ++pass) {
                 const int shift = pass == 1 ? 10 : 0;
                 const uint32_t nb = pass == 1 ? 2048u : 1024u;
-                for (uint32_t b = tid; b < nb; b += kTopkThreads) s.hist[b] = 0;
-                __syncthreads();
-                topk_for_row(x, N, [&](int, float v, bool valid) {
+                for (uint32_t b = tid; b < nb; b += NT) s.hist[b] = 0;
+                topk_sync<NT>();
+                topk_for_row<NT>(x, N, [&](int, float v, bool valid) {
                     bool in = valid && topk_eligible(v);
                     const uint32_t key = in ? topk_key(v) : 0u;
                     in = in && (key & pmask) == prefix;
                     topk_hist_add(s.hist, (key >> shift) & (nb - 1), in);
                 });
-                __syncthreads();
+                topk_sync<NT>();
                 topk_find_bin(s, s.hist, nb, kk);
                 kk -= s.sel_above;
                 prefix |= s.sel_bin << shift;
                 pmask |= (nb - 1) << shift;
                 tie_total = s.sel_count;
-                __syncthreads();
+                topk_sync<NT>();
             }
             const uint32_t T = prefix;  // the k-th largest key; kk of the entries equal to it
             const bool ordered_ties = kk < tie_total;
@@ -459,27 +513,27 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkParams 
                     // rank of this tie among the row's ties, in index order (the in-order
                     // visit gives one element per thread per call, threads in index order)
                     uint32_t step_ties = 0;
-                    const uint32_t incl = topk_block_scan(tie ? 1u : 0u, s.scratch, step_ties);
+                    const uint32_t incl = topk_block_scan<NT>(tie ? 1u : 0u, s.scratch, step_ties);
                     const uint32_t rank = s.tie_base + incl - (tie ? 1u : 0u);
                     take = greater || (tie && rank < kk);
-                    __syncthreads();
+                    topk_sync<NT>();
                     if (tid == 0) s.tie_base += step_ties;
                 }
                 topk_append(s.cand, &s.n_cand, topk_composite(key, i), take);
             };
             if (ordered_ties)
-                topk_for_row<true>(x, N, collect);
+                topk_for_row<NT, true>(x, N, collect);
             else
-                topk_for_row(x, N, collect);
-            __syncthreads();
+                topk_for_row<NT>(x, N, collect);
+            topk_sync<NT>();
         }
 
         // ---- 4. order the winners and write the row
         const int n_sel = int(s.n_cand);
-        topk_sort_any(s.cand, n_sel);
+        topk_sort_any<NT>(s.cand, n_sel);
         int32_t* oi = p.indices + row * int64_t(k);
         float* ov = p.values ? p.values + row * int64_t(k) : nullptr;
-        for (int j = tid; j < k; j += kTopkThreads) {
+        for (int j = tid; j < k; j += NT) {
             int32_t idx = -1;
             float val = __int_as_float(0xff800000);
             if (j < n_sel) {
@@ -498,7 +552,7 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkParams 
             oi[j] = idx;
             if (ov) ov[j] = val;
         }
-        __syncthreads();
+        topk_sync<NT>();
     }
 }
 
