@@ -80,7 +80,10 @@ void init_device(int dev, DeviceState& st)
         cudaFuncSetAttribute(topk_kernel<TopkSmemOne>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              int(sizeof(TopkSmemOne))) != cudaSuccess ||
         cudaFuncSetAttribute(topk_kernel<TopkSmemPair>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             int(2 * sizeof(TopkSmemPair))) != cudaSuccess) {
+                             int(2 * sizeof(TopkSmemPair))) != cudaSuccess ||
+        cudaFuncSetAttribute(topk_kernel<TopkSmemPairWide>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(2 * sizeof(TopkSmemPairWide))) != cudaSuccess) {
         st.init_status = FP8MQA_ERR_LAUNCH;
         return;
     }
@@ -562,13 +565,17 @@ int fp8_mqa_topk(const float* logits, int64_t M, int64_t N, int64_t ld, int32_t 
     p.indices = indices;
     p.values = values;
     // At most one CTA per SM, each walking rows: the rows in flight stay resident in L2 for
-    // the select's re-reads.  Rows of up to 32768 keys with k <= 512 go two per CTA.
+    // the select's re-reads.  Rows of up to 32768 keys go two per CTA.
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int64_t pair_grid = (M + 1) / 2 < st->sm_count ? (M + 1) / 2 : st->sm_count;
     if (N <= 32768 && k <= 512) {
-        const int64_t ctas = (M + 1) / 2;
-        const int64_t grid = ctas < st->sm_count ? ctas : st->sm_count;
-        fp8mqa::topk_kernel<fp8mqa::TopkSmemPair><<<dim3(uint32_t(grid)), fp8mqa::kTopkThreads,
+        fp8mqa::topk_kernel<fp8mqa::TopkSmemPair><<<dim3(uint32_t(pair_grid)),
+                                                      fp8mqa::kTopkThreads,
                                                       2 * sizeof(fp8mqa::TopkSmemPair), s>>>(p);
+    } else if (N <= 32768) {
+        fp8mqa::topk_kernel<fp8mqa::TopkSmemPairWide><<<dim3(uint32_t(pair_grid)),
+                                                          fp8mqa::kTopkThreads,
+                                                          2 * sizeof(fp8mqa::TopkSmemPairWide), s>>>(p);
     } else {
         const int64_t grid = M < st->sm_count ? M : st->sm_count;
         fp8mqa::topk_kernel<fp8mqa::TopkSmemOne><<<dim3(uint32_t(grid)), fp8mqa::kTopkThreads,

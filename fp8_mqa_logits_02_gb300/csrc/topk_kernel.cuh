@@ -8,9 +8,9 @@
 // equals +0.0); slots past the row's finite entries get index -1 and value -inf.
 //
 // A persistent grid of at most one CTA per SM walks the rows (a row's second read comes from
-// L2): rows of up to 32768 keys with k <= 512 two at a time, 256 threads each on a named
-// barrier of their own, so one row's barrier waits overlap the other's work; other rows one
-// at a time with all 512 threads.  Radix select on an order-preserving 32-bit key:
+// L2): rows of up to 32768 keys two at a time, 256 threads each on a named barrier of their
+// own, so one row's barrier waits overlap the other's work; longer rows one at a time with
+// all 512 threads.  Radix select on an order-preserving 32-bit key:
 //   1. read the row, histogram the top 11 key bits (a private histogram per warp, so hot
 //      bins do not serialise the whole block);
 //   2. the bin b0 holding the k-th largest is found from the top;
@@ -42,29 +42,33 @@ struct TopkParams {
 // A CTA works on kTopkThreads / NT rows at once, NT threads each, a row's threads
 // synchronising on a named barrier of their own (the whole CTA's barrier when NT is the
 // CTA).  One row's shared memory; TIE entries of the threshold bin (and the bins above it)
-// are selected in it.
-template <int NT, int TIE>
+// are selected in it; its warps share HW first-pass histograms.
+template <int NT, int TIE, int HW = NT / 32>
 struct TopkSmem {
     static constexpr int kNT = NT;
     static constexpr int kTie = TIE;
-    uint32_t whist[NT / 32][kTopkBins];  // per-warp histograms, later the spare buffer
+    static constexpr int kHW = HW;
+    uint32_t whist[HW][kTopkBins];  // first-pass histograms, later the spare buffer
     uint32_t hist[kTopkBins];
     unsigned long long cand[kTopkMaxK];
     unsigned long long tbuf[TIE];
     uint32_t scratch[NT / 32];
     uint32_t sel_bin, sel_above, sel_count, n_cand, n_tie, tie_base, n_spare, pad;
 };
-// Rows of up to 32768 keys with k <= 512: two rows per CTA, 256 threads each.  Otherwise one
-// row per CTA with the larger threshold-bin buffer that long rows and k = 2048 need.
+// Rows of up to 32768 keys go two per CTA, 256 threads each: with k <= 512 a 2048-entry
+// threshold-bin buffer and a histogram per warp, with larger k a 4096-entry buffer and a
+// histogram per two warps.  Longer rows go one per CTA with the 8192-entry buffer they need.
 using TopkSmemPair = TopkSmem<256, 2048>;
+using TopkSmemPairWide = TopkSmem<256, 4096, 4>;
 using TopkSmemOne = TopkSmem<512, 8192>;
-constexpr uint32_t kTopkSmemBytes = sizeof(TopkSmemOne) > 2 * sizeof(TopkSmemPair)
-                                        ? uint32_t(sizeof(TopkSmemOne))
-                                        : uint32_t(2 * sizeof(TopkSmemPair));
-static_assert(kTopkSmemBytes <= 232448, "top-k shared memory");
-static_assert(sizeof(TopkSmemPair) % 16 == 0, "row slices stay 16-byte aligned");
-static_assert(TopkSmemPair::kTie <= TopkSmemPair::kNT / 32 * kTopkBins / 2 &&
-                  TopkSmemOne::kTie <= TopkSmemOne::kNT / 32 * kTopkBins / 2,
+static_assert(sizeof(TopkSmemOne) <= 232448 && 2 * sizeof(TopkSmemPair) <= 232448 &&
+                  2 * sizeof(TopkSmemPairWide) <= 232448,
+              "top-k shared memory");
+static_assert(sizeof(TopkSmemPair) % 16 == 0 && sizeof(TopkSmemPairWide) % 16 == 0,
+              "row slices stay 16-byte aligned");
+static_assert(TopkSmemPair::kTie <= TopkSmemPair::kHW * kTopkBins / 2 &&
+                  TopkSmemPairWide::kTie <= TopkSmemPairWide::kHW * kTopkBins / 2 &&
+                  TopkSmemOne::kTie <= TopkSmemOne::kHW * kTopkBins / 2,
               "the spare buffer holds the threshold-bin buffer");
 
 // This thread's index among its row's NT threads, and the row's barrier.
@@ -413,15 +417,21 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkParams 
     const int tid = topk_tid<NT>(), warp = tid >> 5;
     const int N = int(p.N);
     const int k = p.k;
-    uint32_t* const my_hist = s.whist[warp];
+    uint32_t* const my_hist = s.whist[warp % S::kHW];
 
     for (int64_t row = int64_t(blockIdx.x) * kRowsPerCta + slot; row < p.M;
          row += int64_t(gridDim.x) * kRowsPerCta) {
         const float* x = p.logits + row * p.ld;
 
         // ---- 1. top 11 key bits, one histogram per warp, then their sum
-        for (int b = tid & 31; b < kTopkBins; b += 32) my_hist[b] = 0;
-        __syncwarp();
+        if constexpr (S::kHW == NT / 32) {
+            for (int b = tid & 31; b < kTopkBins; b += 32) my_hist[b] = 0;
+            __syncwarp();
+        } else {
+            // warps share histograms: all of them are cleared before any warp counts
+            for (int b = tid; b < S::kHW * kTopkBins; b += NT) (&s.whist[0][0])[b] = 0;
+            topk_sync<NT>();
+        }
         topk_for_row<NT>(x, N, [&](int, float v, bool valid) {
             const bool in = valid && topk_eligible(v);
             topk_hist_add(my_hist, in ? (topk_key(v) >> 21) : 0u, in);
@@ -430,7 +440,7 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkParams 
         for (int b = tid; b < kTopkBins; b += NT) {
             uint32_t h = 0;
 #pragma unroll
-            for (int w = 0; w < NT / 32; ++w) h += s.whist[w][b];
+            for (int w = 0; w < S::kHW; ++w) h += s.whist[w][b];
             s.hist[b] = h;
         }
         if (tid == 0) {
