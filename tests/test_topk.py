@@ -100,7 +100,7 @@ def test_indexer_pipeline_top512_matches_the_oracle_pipeline():
     assert same >= 0.9 * len(rows) and overlap >= 500, (same, overlap)
 
 
-@pytest.mark.parametrize("N", [3000, 20000])
+@pytest.mark.parametrize("N", [3000, 20000, 40000])
 def test_crowded_threshold_bin_takes_the_multi_pass_path(N):
     # more entries than the threshold-bin buffer holds (1024 per warp of the row's group,
     # at most 8192) share the top 11 key bits of the k-th largest: the select resolves the
