@@ -17,7 +17,8 @@
 //   3. read the row again and append the keys of b0 and above to a shared-memory buffer
 //      (one append per key); those above b0 are winners, and two more radix passes (key
 //      bits 20..10 and 9..0) over those of b0 pick the rest, equal keys taken by index;
-//   4. the winners (at most 2048) are sorted by a bitonic network and written.
+//   4. the winners (at most 2048) are sorted (each warp sorts a run in registers, then the
+//      runs are merged pairwise) and written.
 // When b0 and the bins above hold more entries than the buffer, the remaining 21 key bits
 // of b0 are resolved by two more histogram passes over the row and a collect pass that
 // takes the ties in index order.
@@ -406,6 +407,106 @@ __device__ __forceinline__ void topk_sort_any(unsigned long long* buf, int n)
     }
 }
 
+// Sort of the winners buf[0, n) descending, NT < n <= NT * E, through tmp (NT * E entries):
+// each warp sorts its run of 32 * E entries in registers (strides below E in the thread, the
+// rest by shuffles, no barrier), then the runs are merged pairwise: every thread finds where
+// its E outputs start on its merge diagonal by binary search and merges them in sequence.
+// Buffers ping-pong between buf and tmp, the result ends in buf; zeros pad past n.
+template <int NT, int E>
+__device__ __forceinline__ void topk_sort_merge(unsigned long long* buf, unsigned long long* tmp,
+                                                int n)
+{
+    constexpr int R = 32 * E;  // one warp's run
+    constexpr int P = NT * E;
+    const int tid = topk_tid<NT>();
+    const int lane = tid & 31, warp = tid >> 5;
+    {
+        unsigned long long v[E];
+#pragma unroll
+        for (int j = 0; j < E; ++j) {
+            const int e = warp * R + lane * E + j;
+            v[j] = e < n ? buf[e] : 0ull;
+        }
+#pragma unroll
+        for (int size = 2; size <= R; size <<= 1) {
+#pragma unroll
+            for (int stride = size >> 1; stride > 0; stride >>= 1) {
+                if (stride >= E) {
+#pragma unroll
+                    for (int j = 0; j < E; ++j) {
+                        const int e = lane * E + j;
+                        const unsigned long long o = __shfl_xor_sync(0xffffffffu, v[j], stride / E);
+                        const bool keep_max = ((e & size) == 0) == ((e & stride) == 0);
+                        v[j] = (o > v[j]) == keep_max ? o : v[j];
+                    }
+                } else if (stride == 1) {
+                    topk_sort_in_thread<E, 1>(v, lane, size);
+                } else if (stride == 2) {
+                    topk_sort_in_thread<E, 2>(v, lane, size);
+                } else {
+                    topk_sort_in_thread<E, 4>(v, lane, size);
+                }
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < E; ++j) buf[warp * R + lane * E + j] = v[j];
+    }
+    topk_sync<NT>();
+    unsigned long long* src = buf;
+    unsigned long long* dst = tmp;
+    for (int L = R; L < P; L <<= 1) {
+        // runs [base, base + L) and [base + L, base + 2L) merge into dst[base, base + 2L)
+        const int o0 = tid * E;
+        const int base = o0 & ~(2 * L - 1);
+        const int d = o0 - base;
+        const unsigned long long* A = src + base;
+        const unsigned long long* B = src + base + L;
+        int lo = d > L ? d - L : 0, hi = d < L ? d : L;
+        while (lo < hi) {  // how many of the first d outputs come from A
+            const int mid = (lo + hi) >> 1;
+            if (A[mid] > B[d - 1 - mid])
+                lo = mid + 1;
+            else
+                hi = mid;
+        }
+        int i = lo, j = d - lo;
+#pragma unroll
+        for (int q = 0; q < E; ++q) {
+            const bool take_a = j >= L || (i < L && A[i] > B[j]);
+            dst[o0 + q] = take_a ? A[i++] : B[j++];
+        }
+        topk_sync<NT>();
+        unsigned long long* t = src;
+        src = dst;
+        dst = t;
+    }
+    if (src != buf) {
+        for (int e = tid; e < n; e += NT) buf[e] = src[e];
+        topk_sync<NT>();
+    }
+}
+
+// The winners' sort: in registers for up to NT entries, by runs and merges beyond.
+template <int NT>
+__device__ __forceinline__ void topk_sort_winners(unsigned long long* buf, unsigned long long* tmp,
+                                                  int n)
+{
+    if (n <= NT)
+        topk_sort_desc_reg<NT, 1>(buf, n);
+    else if (n <= 2 * NT)
+        topk_sort_merge<NT, 2>(buf, tmp, n);
+    else if (n <= 4 * NT)
+        topk_sort_merge<NT, 4>(buf, tmp, n);
+    else if constexpr (NT * 8 <= kTopkMaxK) {
+        if (n <= 8 * NT)
+            topk_sort_merge<NT, 8>(buf, tmp, n);
+        else
+            topk_sort_desc<NT>(buf, n);
+    } else {
+        topk_sort_desc<NT>(buf, n);
+    }
+}
+
 template <typename S>
 __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkParams p)
 {
@@ -540,7 +641,7 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkParams 
 
         // ---- 4. order the winners and write the row
         const int n_sel = int(s.n_cand);
-        topk_sort_any<NT>(s.cand, n_sel);
+        topk_sort_winners<NT>(s.cand, reinterpret_cast<unsigned long long*>(&s.whist[0][0]), n_sel);
         int32_t* oi = p.indices + row * int64_t(k);
         float* ov = p.values ? p.values + row * int64_t(k) : nullptr;
         for (int j = tid; j < k; j += NT) {
