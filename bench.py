@@ -7,18 +7,25 @@ flushed (a 256 MiB write) before every timed call, and each call is timed on the
 launching stream with CUDA events.  The metric is valid-window FP8 TFLOP/s:
 2*H*D*sum_m |window_m| per call over the call's device time.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-                  [--impl reference] [--no-cpu-baseline]
+The same JSON line carries a "workloads" block: every other configuration of the page's
+kernel-time table (and the clean_logits = 0 and explicit-split variants) timed the same
+way, so that each figure quoted for them comes from this run.
 
-``--impl reference`` times the CPU oracle (test infrastructure) on the host cores on
-a bounded sample of the same workload and prints the same JSON line with
-"impl": "reference".
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                  [--impl reference] [--no-cpu-baseline] [--no-workloads]
+
+``--gpus N`` with N > 1 outside torchrun starts N replica ranks itself (one per GPU,
+through torch.distributed.run); under torchrun each rank runs the same full call and the
+job time is the slowest rank's.  ``--impl reference`` times the CPU oracle (test
+infrastructure) on the host cores on a bounded sample of the same workload and prints the
+same JSON line with "impl": "reference".
 """
 from __future__ import annotations
 
 import argparse
 import json
 import os
+import socket
 import statistics
 import subprocess
 import sys
@@ -41,9 +48,37 @@ FALLBACK_BF16_TFLOPS = 1900.0
 FP8_OVER_BF16 = 2.0  # nominal dense ratio 4.5 / 2.25 PFLOP/s
 REFERENCE_BUDGET_S = 90.0  # CPU seconds for a whole --impl reference run
 
+# The per-workload block: (workload, clean_logits, split_n); split_n 0 is the default.
+WORKLOAD_TABLE = [
+    ("tiny_causal_64x256", 1, 0),
+    ("causal_8192x8192", 0, 0),
+    ("chunk_causal_4096x32768", 1, 0),
+    ("chunk_causal_4096x32768", 0, 0),
+    ("chunk_causal_2048x65536", 1, 0),
+    ("long_causal_1024x131072", 1, 0),
+    ("kpool_causal_16384x32000", 1, 0),
+    ("cp_4096x32768", 1, 0),
+    ("multi_req_4096x32768", 1, 0),
+    ("multi_req_4096x32768", 1, 20),
+    ("multi_req_4096x32768", 0, 0),
+    ("multi_req_2048x65536", 1, 0),
+    ("multi_req_1024x131072", 1, 0),
+    ("multi_req_1024x131072", 1, 20),
+    ("multi_req_8192x8192", 1, 0),
+]
+
 
 def valid_flops(inp) -> float:
     return 2.0 * inp["H"] * inp["D"] * workloads.valid_pairs(inp["ks"], inp["ke"], inp["N"])
+
+
+def algorithmic_bytes(inp, clean: int) -> float:
+    """HBM bytes one call must move: the logits it writes (every entry with clean_logits=1,
+    the in-window ones with 0), Q and w once, K and kv_scale once, ks and ke."""
+    M, N, H, D = inp["M"], inp["N"], inp["H"], inp["D"]
+    pairs = workloads.valid_pairs(inp["ks"], inp["ke"], N)
+    out = 4.0 * (M * N if clean else pairs)
+    return out + M * H * D + M * H * 4 + N * (D + 4) + 8.0 * M
 
 
 def load_peaks():
@@ -71,6 +106,7 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
+        self.lines = []
 
     def __enter__(self):
         try:
@@ -142,6 +178,20 @@ def max_over_ranks(value: float, world: int) -> float:
     return float(t.item())
 
 
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def replica_command(gpus: int, argv, port: int | None = None):
+    """The torch.distributed.run command that starts `gpus` replica ranks of this script
+    with the same arguments (one process per GPU, rendezvous on 127.0.0.1)."""
+    return [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+            f"--nproc-per-node={gpus}", "--master-addr=127.0.0.1",
+            f"--master-port={port or _free_port()}", os.path.abspath(__file__), *argv]
+
+
 def cpu_oracle_sample(inp, budget_rows: int, threads: int):
     """Time the oracle on an evenly spaced sample of query rows; returns TFLOP/s etc."""
     import oracle
@@ -184,8 +234,8 @@ def run_reference(args):
         "ms_per_step": 1e3 * secs / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": wl.name, "M": wl.M, "N": wl.N, "H": wl.H, "D": wl.D,
-                   "windows": "causal: ks=0, ke=N-M+m+1", "clean_logits": 1,
-                   "l2": "n/a (CPU)"},
+                   "windows": workloads.describe(wl), "clean_logits": int(args.clean),
+                   "split_n": args.split_n, "l2": "n/a (CPU)"},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                          "sample": f"{samples[0]['rows']} query rows per step (every "
                                    f"{samples[0]['stride']}th row) of {wl.name}, fp64 C "
@@ -195,6 +245,76 @@ def run_reference(args):
     }
     print(json.dumps(line), flush=True)
     return 0
+
+
+def _device_inputs(inp, dev):
+    import torch
+    return (torch.from_numpy(inp["q"]).to(dev).view(torch.float8_e4m3fn),
+            torch.from_numpy(inp["k"]).to(dev).view(torch.float8_e4m3fn),
+            torch.from_numpy(inp["kv_scale"]).to(dev), torch.from_numpy(inp["w"]).to(dev),
+            torch.from_numpy(inp["ks"]).to(dev), torch.from_numpy(inp["ke"]).to(dev))
+
+
+def time_calls(fm, args_dev, out, clean, split_n, steps, warmup, flush, stream, dev):
+    """Mean device time (ms) of `steps` calls, each after an L2 flush, CUDA events on the
+    launching stream; plus the clocks sampled meanwhile."""
+    import torch
+
+    def call():
+        fm.fp8_mqa_logits(*args_dev, out=out, clean_logits=bool(clean), split_n=split_n,
+                          stream=stream)
+
+    for _ in range(warmup):
+        flush.zero_()
+        call()
+    torch.cuda.synchronize(dev)
+    if fm.check_error(stream) != 0:
+        raise RuntimeError("device status after warm-up is not OK")
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    torch.cuda.synchronize(dev)
+    with ClockSampler(dev.index) as clocks:
+        for i in range(steps):
+            flush.zero_()
+            starts[i].record(stream)
+            call()
+            ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+    status = fm.check_error(stream)
+    if status != 0:
+        raise RuntimeError(f"device status {fm.strerror(status)}")
+    return [s.elapsed_time(e) for s, e in zip(starts, ends)], clocks.summary()
+
+
+def workload_block(fm, dev, stream, flush, steps, warmup, fp8_peak, hbm_peak, sm_count):
+    """Every configuration of WORKLOAD_TABLE timed like the headline call."""
+    import torch
+    rows = []
+    cache = {}
+    for name, clean, split_n in WORKLOAD_TABLE:
+        wl = workloads.WORKLOADS[name]
+        if name not in cache:
+            cache.clear()
+            torch.cuda.empty_cache()
+            inp = workloads.make(wl)
+            cache[name] = (inp, _device_inputs(inp, dev))
+        inp, args_dev = cache[name]
+        out = torch.empty((inp["M"], inp["N"]), dtype=torch.float32, device=dev)
+        ms, clocks = time_calls(fm, args_dev, out, clean, split_n, steps, warmup, flush,
+                                stream, dev)
+        del out
+        mean_s = statistics.mean(ms) * 1e-3
+        flops = valid_flops(inp)
+        nbytes = algorithmic_bytes(inp, clean)
+        split_used = split_n or fm.default_split(inp["M"], inp["N"], sm_count)
+        rows.append({
+            "workload": name, "windows": workloads.describe(wl), "clean_logits": clean,
+            "split_n": split_n, "split_used": split_used, "steps": steps,
+            "us_per_call": mean_s * 1e6, "us_min": min(ms) * 1e3,
+            "tflops": flops / mean_s / 1e12, "frac_of_fp8_peak": flops / mean_s / 1e12 / fp8_peak,
+            "hbm_gbs": nbytes / mean_s / 1e9, "frac_of_hbm": nbytes / mean_s / 1e9 / hbm_peak,
+            "clocks": clocks})
+    return rows
 
 
 def run_gpu(args):
@@ -210,50 +330,23 @@ def run_gpu(args):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     fm.lib()
+    sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
 
     wl = workloads.WORKLOADS[args.workload]
     inp = workloads.make(wl)
     M, N, H, D = inp["M"], inp["N"], inp["H"], inp["D"]
     flops = valid_flops(inp)
-    q = torch.from_numpy(inp["q"]).to(dev).view(torch.float8_e4m3fn)
-    k = torch.from_numpy(inp["k"]).to(dev).view(torch.float8_e4m3fn)
-    kv = torch.from_numpy(inp["kv_scale"]).to(dev)
-    w = torch.from_numpy(inp["w"]).to(dev)
-    ks = torch.from_numpy(inp["ks"]).to(dev)
-    ke = torch.from_numpy(inp["ke"]).to(dev)
+    args_dev = _device_inputs(inp, dev)
     out = torch.empty((M, N), dtype=torch.float32, device=dev)
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def step():
-        fm.fp8_mqa_logits(q, k, kv, w, ks, ke, out=out, clean_logits=bool(args.clean),
-                          split_n=args.split_n, stream=stream)
-
-    for _ in range(args.warmup):
-        flush.zero_()
-        step()
-    torch.cuda.synchronize(dev)
-    if fm.check_error(stream) != 0:
-        raise RuntimeError("device status after warm-up is not OK")
-
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     if ws > 1:
         torch.distributed.barrier()
-    torch.cuda.synchronize(dev)
-    with ClockSampler(dev.index) as clocks:
-        for i in range(args.steps):
-            flush.zero_()
-            starts[i].record(stream)
-            step()
-            ends[i].record(stream)
-        torch.cuda.synchronize(dev)
+    ms, clocks = time_calls(fm, args_dev, out, args.clean, args.split_n, args.steps,
+                            args.warmup, flush, stream, dev)
     if ws > 1:
         torch.distributed.barrier()
-    status = fm.check_error(stream)
-    if status != 0:
-        raise RuntimeError(f"device status {fm.strerror(status)}")
-    ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     total_ms = max_over_ranks(sum(ms), ws)
     value = flops * args.steps * ws / (total_ms * 1e-3) / 1e12
     per_launch_s = statistics.mean(ms) * 1e-3
@@ -294,6 +387,7 @@ def run_gpu(args):
     e2e_value = flops * e2e_steps * ws / (e2e_ms * 1e-3) / 1e12
     if fm.check_error(stream) != 0:
         raise RuntimeError("device status after e2e is not OK")
+    del wsp, hout
 
     peaks = load_peaks()
     fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
@@ -316,8 +410,9 @@ def run_gpu(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "fp8e4m3*fp8e4m3->f32", "data": "synthetic",
         "config": {"workload": wl.name, "M": M, "N": N, "H": H, "D": D,
-                   "windows": "causal: ks=0, ke=N-M+m+1" if wl.windows == "causal" else
-                   wl.windows, "clean_logits": int(args.clean), "split_n": args.split_n,
+                   "windows": workloads.describe(wl), "clean_logits": int(args.clean),
+                   "split_n": args.split_n,
+                   "split_used": args.split_n or fm.default_split(M, N, sm_count),
                    "valid_flops_per_call": flops,
                    "l2": f"flushed before every timed call ({FLUSH_BYTES >> 20} MiB write)",
                    "timing": "CUDA events per call on the launching stream"},
@@ -325,13 +420,16 @@ def run_gpu(args):
                      "unit": "TFLOP/s", "frac": achieved / fp8_peak, "traffic": traffic,
                      "peak_source": f"{peaks['source']} bf16 burst x {FP8_OVER_BF16:g} "
                                     "(nominal fp8/bf16 ratio)",
-                     "kernel": "fp8_mqa_logits_kernel"},
+                     "kernel": "fp8_mqa_logits_kernel", "kernel_rev": KERNEL_REV},
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                 "entry": "fp8_mqa_logits_host (pinned host buffers)"},
         "gpu_launches": args.steps,
-        "clocks": clocks.summary(),
+        "clocks": clocks,
     }
+    if ws == 1 and not args.no_workloads:
+        line["workloads"] = workload_block(fm, dev, stream, flush, min(args.steps, 20),
+                                           args.warmup, fp8_peak, peaks["hbm_gbs"], sm_count)
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         import oracle
         oracle.build()
@@ -398,10 +496,10 @@ def run_topk(args):
 
 
 # Revision tag of the kernel the committed ncu traffic figure was taken on.
-KERNEL_REV = "v5"
+KERNEL_REV = "v6"
 
 
-def main(argv=None):
+def parse_args(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
@@ -411,6 +509,8 @@ def main(argv=None):
     ap.add_argument("--split-n", type=int, default=0)
     ap.add_argument("--impl", default="native", choices=("native", "reference"))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the per-workload block (the headline call only)")
     ap.add_argument("--topk", type=int, default=0,
                     help="time the per-row top-k (this k) over the workload's logits instead")
     ap.add_argument("--reference-rows", type=int, default=4096,
@@ -418,6 +518,21 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
+    return args
+
+
+def main(argv=None):
+    argv = list(sys.argv[1:] if argv is None else argv)
+    args = parse_args(argv)
+    if args.gpus < 1:
+        raise SystemExit("--gpus must be at least 1")
+    ws, _, _ = dist_env()
+    if "WORLD_SIZE" in os.environ:
+        if ws != args.gpus:
+            raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE={ws}: launch one rank per GPU")
+    elif args.gpus > 1:
+        # replicas: one rank per GPU, each running the same full call
+        return subprocess.call(replica_command(args.gpus, argv))
     if args.impl == "reference":
         return run_reference(args)
     if args.topk:

@@ -27,12 +27,16 @@ STATUS = {
     -5: "FP8MQA_ERR_LAUNCH",
     -6: "FP8MQA_ERR_TIMEOUT",
     -7: "FP8MQA_ERR_CUDA",
+    -8: "FP8MQA_ERR_BOUNDS",
+    -9: "FP8MQA_ERR_CAPACITY",
 }
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libfp8mqa.so")
+DEBUG_LIB_PATH = os.path.join(_HERE, "libfp8mqa_debug.so")
 _lock = threading.Lock()
-_lib = None
+_libs = {}
+_debug = False
 
 # Every symbol the C header declares, with its ctypes signature.
 _P = ctypes.c_void_p
@@ -40,9 +44,10 @@ _I64, _I32, _U64 = ctypes.c_int64, ctypes.c_int32, ctypes.c_uint64
 SIGNATURES = {
     "fp8_mqa_logits": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I32, _I32, _I32,
                                       _I32, _P]),
-    "fp8_mqa_logits_is_supported": (ctypes.c_int, [_I64, _I64, _I32, _I32]),
+    "fp8_mqa_logits_is_supported": (ctypes.c_int, [_I64, _I64, _I32, _I32, _I32]),
     "fp8_mqa_logits_default_split": (ctypes.c_int, [_I64, _I64, _I32]),
     "fp8_mqa_logits_check_error": (ctypes.c_int, [_P]),
+    "fp8_mqa_logits_set_wait_limit_ns": (ctypes.c_uint64, [_U64]),
     "fp8_mqa_logits_host_workspace_bytes": (ctypes.c_uint64, [_I64, _I64, _I32, _I32]),
     "fp8_mqa_logits_host": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I32, _I32,
                                            _I32, _I32, _P, _U64, _P]),
@@ -61,28 +66,39 @@ class Fp8MqaError(RuntimeError):
         super().__init__(f"{what}: {strerror(status)} ({status})")
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile ``libfp8mqa.so`` in-tree with nvcc for sm_103a."""
+def build(force: bool = False, verbose: bool = False, debug: bool | None = None) -> str:
+    """Compile ``libfp8mqa.so`` (and, by default, its bounds-checking variant) in-tree with
+    nvcc for sm_103a."""
     from . import nvcc_build
-    return nvcc_build.build(force=force, verbose=verbose)
+    return nvcc_build.build(force=force, verbose=verbose, debug=debug)
 
 
-def lib():
-    """The loaded library; raises if it has not been built."""
-    global _lib
+def use_debug_library(on: bool) -> None:
+    """Route every later call of this module through ``libfp8mqa_debug.so``, the build whose
+    kernel checks each global access first and records a violation (``check_error`` then
+    returns FP8MQA_ERR_BOUNDS) instead of making it; ``False`` switches back."""
+    global _debug
+    _debug = bool(on)
+
+
+def lib(debug: bool | None = None):
+    """The loaded library (the bounds-checking build when selected); raises if it has not
+    been built."""
+    dbg = _debug if debug is None else bool(debug)
+    path = DEBUG_LIB_PATH if dbg else LIB_PATH
     with _lock:
-        if _lib is None:
-            if not os.path.exists(LIB_PATH):
+        if path not in _libs:
+            if not os.path.exists(path):
                 raise RuntimeError(
-                    f"{LIB_PATH} is missing: build it with "
+                    f"{path} is missing: build it with "
                     "`python -m fp8_mqa_logits_02_gb300.nvcc_build` (there is no CPU fallback)")
-            handle = ctypes.CDLL(LIB_PATH)
+            handle = ctypes.CDLL(path)
             for name, (res, args) in SIGNATURES.items():
                 fn = getattr(handle, name)
                 fn.restype = res
                 fn.argtypes = args
-            _lib = handle
-    return _lib
+            _libs[path] = handle
+    return _libs[path]
 
 
 def strerror(status: int) -> str:
@@ -92,8 +108,16 @@ def strerror(status: int) -> str:
         return STATUS.get(int(status), f"unknown status {status}")
 
 
-def is_supported(M: int, N: int, H: int = HEADS, D: int = DIM) -> bool:
-    return bool(lib().fp8_mqa_logits_is_supported(M, N, H, D))
+def is_supported(M: int, N: int, H: int = HEADS, D: int = DIM, device: int = -1) -> bool:
+    """Whether (M, N, H, D) is inside the contract; with ``device >= 0`` also whether that
+    CUDA device is a compute-capability 10.3 GPU."""
+    return bool(lib().fp8_mqa_logits_is_supported(M, N, H, D, int(device)))
+
+
+def set_wait_limit_ns(ns: int) -> int:
+    """Limit of one on-device pipeline wait for later launches (0: the 1 s default).
+    Returns the previous limit.  For diagnostics and tests of the failure path."""
+    return int(lib().fp8_mqa_logits_set_wait_limit_ns(int(ns)))
 
 
 def default_split(M: int, N: int, num_sms: int) -> int:

@@ -8,6 +8,7 @@
 #include <atomic>
 #include <algorithm>
 #include <cstdint>
+#include <cstdio>
 #include <cstring>
 #include <functional>
 #include <mutex>
@@ -20,16 +21,27 @@ namespace fp8mqa {
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr uint32_t kSchedSlots = 64;        // concurrent launches per device before reuse
-constexpr uint64_t kTimeoutNs = 1000000000ull;  // bounded device waits give up after 1 s
+// Scheduler slots: a ring for direct launches (a slot is reused every kSchedSlots launches)
+// and one slot of its own for every launch captured into a CUDA graph (never reused, since a
+// graph's kernel keeps its slot for every replay).
+constexpr uint32_t kSchedSlots = 256;
+constexpr uint32_t kGraphSlots = 16384;
+constexpr uint64_t kDefaultWaitNs = 1000000000ull;  // bounded device waits give up after 1 s
+constexpr uint64_t kDrainNs = 1000000000ull;        // bound of the drain before a CTA exits
+constexpr uint64_t kHintedWaitNs = 100000ull;       // shorter limits also bound each suspension
+constexpr size_t kStatusBytes = 256;                // status word + first bounds violation
+
+std::atomic<uint64_t> g_wait_ns{kDefaultWaitNs};
 
 struct DeviceState {
     std::once_flag once;
     int init_status = FP8MQA_OK;
+    std::atomic<bool> ready{false};
     int sm_count = 0;
-    SchedSlot* sched = nullptr;  // kSchedSlots slots, zeroed
-    int32_t* status = nullptr;   // one status word
+    SchedSlot* sched = nullptr;  // kSchedSlots ring slots, then kGraphSlots graph slots, zeroed
+    int32_t* status = nullptr;   // status word (+ bounds record)
     std::atomic<uint32_t> seq{0};
+    std::atomic<uint32_t> graph_seq{0};
 };
 
 DeviceState g_dev[kMaxDevices];
@@ -88,7 +100,7 @@ void init_device(int dev, DeviceState& st)
         return;
     }
     void* buf = nullptr;
-    const size_t bytes = kSchedSlots * sizeof(SchedSlot) + 256;
+    const size_t bytes = size_t(kSchedSlots + kGraphSlots) * sizeof(SchedSlot) + kStatusBytes;
     if (cudaMalloc(&buf, bytes) != cudaSuccess) {
         st.init_status = FP8MQA_ERR_CUDA;
         return;
@@ -100,9 +112,13 @@ void init_device(int dev, DeviceState& st)
     }
     st.sched = static_cast<SchedSlot*>(buf);
     st.status = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(buf) +
-                                           kSchedSlots * sizeof(SchedSlot));
+                                           size_t(kSchedSlots + kGraphSlots) * sizeof(SchedSlot));
     std::call_once(g_encode_once, load_encode);
-    if (!g_encode) st.init_status = FP8MQA_ERR_CUDA;
+    if (!g_encode) {
+        st.init_status = FP8MQA_ERR_CUDA;
+        return;
+    }
+    st.ready.store(true, std::memory_order_release);
 }
 
 DeviceState* device_state(int* err)
@@ -140,7 +156,7 @@ int check_args(const uint8_t* q, const uint8_t* k, const float* kv, const float*
 {
     if (M < 0 || N < 0 || split_n < 0 || (clean != 0 && clean != 1))
         return FP8MQA_ERR_INVALID_ARG;
-    if (!fp8_mqa_logits_is_supported(M, N, H, D)) return FP8MQA_ERR_UNSUPPORTED_SHAPE;
+    if (!fp8_mqa_logits_is_supported(M, N, H, D, -1)) return FP8MQA_ERR_UNSUPPORTED_SHAPE;
     if (M == 0 || N == 0) return FP8MQA_OK;
     if (!q || !k || !kv || !w || !ks || !ke || !out) return FP8MQA_ERR_INVALID_ARG;
     if (!aligned(q, 16) || !aligned(k, 16) || !aligned(kv, 16) || !aligned(w, 16) ||
@@ -207,7 +223,9 @@ int enqueue(SchedSlot* sched, int32_t* status, int sm_count, bool clear_sched,
     p.clean = clean;
     p.sched = sched;
     p.status = status;
-    p.timeout_ns = kTimeoutNs;
+    p.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
+    p.drain_ns = kDrainNs;
+    p.suspend_ns = p.wait_ns < kHintedWaitNs ? uint32_t(p.wait_ns > 32 ? p.wait_ns : 32) : 0u;
 
     if (clear_sched && cudaMemsetAsync(sched, 0, sizeof(SchedSlot), stream) != cudaSuccess)
         return FP8MQA_ERR_CUDA;
@@ -224,7 +242,21 @@ int launch(const uint8_t* q, const uint8_t* k, const float* kv, const float* w,
     int err = FP8MQA_OK;
     DeviceState* st = device_state(&err);
     if (!st) return err;
-    SchedSlot* slot = st->sched + (st->seq.fetch_add(1, std::memory_order_relaxed) % kSchedSlots);
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) {
+        cudaGetLastError();
+        return FP8MQA_ERR_CUDA;
+    }
+    SchedSlot* slot;
+    if (cap == cudaStreamCaptureStatusNone) {
+        slot = st->sched + (st->seq.fetch_add(1, std::memory_order_relaxed) % kSchedSlots);
+    } else {
+        // a captured launch keeps its slot for every replay of the graph: give it one that
+        // no other launch uses
+        const uint32_t i = st->graph_seq.fetch_add(1, std::memory_order_relaxed);
+        if (i >= kGraphSlots) return FP8MQA_ERR_CAPACITY;
+        slot = st->sched + kSchedSlots + i;
+    }
     return enqueue(slot, st->status, st->sm_count, false, q, k, kv, w, ks, ke, out, M, N, clean,
                    split_n, stream);
 }
@@ -284,6 +316,7 @@ constexpr size_t kNoAllocStatusOffset = 128;  // status word after the scheduler
 struct NoAllocState {
     std::once_flag once;
     int init_status = FP8MQA_OK;
+    std::atomic<bool> ready{false};
     int sm_count = 0;
     uint8_t* scratch = nullptr;  // device address of no_alloc_scratch on this device
 };
@@ -298,9 +331,9 @@ static __device__ __align__(256) uint8_t no_alloc_scratch[fp8mqa::kNoAllocScratc
 namespace fp8mqa {
 namespace {
 
-// Bytes of the array one call uses: a scheduler slot and the status word.  The need does
-// not grow with M or N; the check below guards the layout against the array size.
-constexpr size_t kNoAllocNeed = kNoAllocStatusOffset + sizeof(int32_t);
+// Bytes of the array one call uses: a scheduler slot, the status word and its bounds record.
+// The need does not grow with M or N; the check below guards the layout against the array size.
+constexpr size_t kNoAllocNeed = kNoAllocStatusOffset + 16;
 static_assert(sizeof(SchedSlot) <= kNoAllocStatusOffset, "scratch layout");
 static_assert(kNoAllocNeed <= kNoAllocScratchBytes, "scratch array too small");
 
@@ -333,7 +366,35 @@ void init_noalloc(int dev, NoAllocState& st)
     }
     st.scratch = static_cast<uint8_t*>(ptr);
     std::call_once(g_encode_once, load_encode);
-    if (!g_encode) st.init_status = FP8MQA_ERR_CUDA;
+    if (!g_encode) {
+        st.init_status = FP8MQA_ERR_CUDA;
+        return;
+    }
+    st.ready.store(true, std::memory_order_release);
+}
+
+// Reads and clears a status word and its bounds record (16 bytes of device memory) after
+// the caller has synchronized; ORs the flags into *flags.  A bounds record (written only by
+// the bounds-checking build) is also reported on stderr.  Allocates nothing.
+bool take_status(int32_t* dev_status, int32_t* flags)
+{
+    uint32_t word[4] = {0, 0, 0, 0};
+    if (cudaMemcpy(word, dev_status, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return false;
+    if (word[0] != 0 || word[2] != 0 || word[3] != 0) {
+        const uint64_t rec = uint64_t(word[2]) | (uint64_t(word[3]) << 32);
+        if (rec != 0)
+            std::fprintf(stderr,
+                         "fp8mqa: bounds violation recorded: kind %u, index %lld "
+                         "(kinds: 1 store, 2 kv_scale, 3 -inf span, 4 K tile, 5 Q block, "
+                         "6 window row, 7 TMEM column)\n",
+                         unsigned(rec >> 48), static_cast<long long>(rec & 0xFFFFFFFFFFFFull));
+        const int32_t zero[4] = {0, 0, 0, 0};
+        if (cudaMemcpy(dev_status, zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+            return false;
+    }
+    *flags |= int32_t(word[0]);
+    return true;
 }
 
 int launch_noalloc(const uint8_t* q, const uint8_t* k, const float* kv, const float* w,
@@ -360,12 +421,23 @@ int launch_noalloc(const uint8_t* q, const uint8_t* k, const float* kv, const fl
 
 extern "C" {
 
-int fp8_mqa_logits_is_supported(int64_t M, int64_t N, int32_t H, int32_t D)
+int fp8_mqa_logits_is_supported(int64_t M, int64_t N, int32_t H, int32_t D, int32_t device)
 {
     if (H != fp8mqa::kHeads || D != fp8mqa::kDim) return 0;
     if (M < 0 || N < 0) return 0;
     if (M * int64_t(H) >= (int64_t(1) << 31)) return 0;
     if (N >= (int64_t(1) << 31)) return 0;
+    if (device >= 0) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device) !=
+                cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device) !=
+                cudaSuccess) {
+            cudaGetLastError();
+            return 0;
+        }
+        if (major != 10 || minor != 3) return 0;
+    }
     return 1;
 }
 
@@ -427,26 +499,38 @@ int fp8_mqa_logits(const uint8_t* q_fp8, const uint8_t* k_fp8, const float* kv_s
 
 int fp8_mqa_logits_check_error(void* stream)
 {
-    int err = FP8MQA_OK;
-    fp8mqa::DeviceState* st = fp8mqa::device_state(&err);
-    if (!st) return err;
-    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= fp8mqa::kMaxDevices) {
+        cudaGetLastError();
         return FP8MQA_ERR_CUDA;
-    int32_t word = 0;
-    if (cudaMemcpy(&word, st->status, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
-        return FP8MQA_ERR_CUDA;
-    if (word != 0) {
-        const int32_t zero = 0;
-        if (cudaMemcpy(st->status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
-            return FP8MQA_ERR_CUDA;
-        return FP8MQA_ERR_TIMEOUT;
     }
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return FP8MQA_ERR_CUDA;
+    }
+    // Only state that earlier calls set up is read: this call allocates nothing.
+    int32_t flags = 0;
+    fp8mqa::DeviceState& st = fp8mqa::g_dev[dev];
+    if (st.ready.load(std::memory_order_acquire) && !fp8mqa::take_status(st.status, &flags))
+        return FP8MQA_ERR_CUDA;
+    fp8mqa::NoAllocState& na = fp8mqa::g_noalloc[dev];
+    if (na.ready.load(std::memory_order_acquire) &&
+        !fp8mqa::take_status(reinterpret_cast<int32_t*>(na.scratch + fp8mqa::kNoAllocStatusOffset),
+                             &flags))
+        return FP8MQA_ERR_CUDA;
+    if (flags & fp8mqa::kStatusBounds) return FP8MQA_ERR_BOUNDS;
+    if (flags & fp8mqa::kStatusTimeout) return FP8MQA_ERR_TIMEOUT;
     return FP8MQA_OK;
+}
+
+uint64_t fp8_mqa_logits_set_wait_limit_ns(uint64_t ns)
+{
+    return fp8mqa::g_wait_ns.exchange(ns ? ns : fp8mqa::kDefaultWaitNs);
 }
 
 uint64_t fp8_mqa_logits_host_workspace_bytes(int64_t M, int64_t N, int32_t H, int32_t D)
 {
-    if (!fp8_mqa_logits_is_supported(M, N, H, D)) return 0;
+    if (!fp8_mqa_logits_is_supported(M, N, H, D, -1)) return 0;
     using fp8mqa::align256;
     const uint64_t m = uint64_t(M), n = uint64_t(N);
     return align256(m * H * D) + align256(n * D) + align256(n * 4) + align256(m * H * 4) +
@@ -597,6 +681,10 @@ const char* fp8_mqa_logits_strerror(int status)
         case FP8MQA_ERR_LAUNCH: return "FP8MQA_ERR_LAUNCH: kernel configuration or launch failed";
         case FP8MQA_ERR_TIMEOUT: return "FP8MQA_ERR_TIMEOUT: a bounded device wait gave up";
         case FP8MQA_ERR_CUDA: return "FP8MQA_ERR_CUDA: CUDA runtime error";
+        case FP8MQA_ERR_BOUNDS:
+            return "FP8MQA_ERR_BOUNDS: a bounds-checking build found an out-of-range access";
+        case FP8MQA_ERR_CAPACITY:
+            return "FP8MQA_ERR_CAPACITY: no scheduler slot left for another captured launch";
         default: return "FP8MQA: unknown status";
     }
 }

@@ -25,20 +25,23 @@
 //               -inf itself").  The spans go out as bulk copies from a shared-memory -inf
 //               buffer, so the TMA engine, not the issue slots the epilogue needs, does them.
 //   warps 4-19  epilogue, four warps per SM sub-partition, two query rows per warp:
-//               thread = one key (TMEM lane), so one tcgen05.ld gives it the 32 heads of
-//               one query row; relu, times w, head sum in registers (no cross-lane
-//               reduction), times kv_scale once per (m, n), then a coalesced store.  Tiles
-//               inside both rows' windows store without compare/select; boundary tiles are
-//               masked (page: "clean stages" vs "masked boundary stages").  kv_scale comes
-//               through the read-only data path, fetched one tile ahead.
+//               thread = one key (TMEM lane), so one tcgen05.ld gives it the 64 values
+//               (row, head) of its two rows; relu, times w, head sum in registers (no
+//               cross-lane reduction), times kv_scale once per (m, n), then a coalesced
+//               store.  Tiles inside both rows' windows store without compare/select;
+//               boundary tiles are masked (page: "clean stages" vs "masked boundary
+//               stages").  kv_scale comes through the read-only path, one tile ahead.
 //
 // Keys sit on the MMA M axis (TMEM lanes) and (row, head) on the N axis: this transposes
 // the page's layout (query heads on the matrix rows) so that the head reduction is a sum
 // inside one thread instead of a cross-lane permutation.
 //
-// Every mbarrier wait is bounded (globaltimer): on expiry the CTA raises a shared abort
-// flag and a global status bit, drains its in-flight TMA and MMA work, frees TMEM and
-// returns.
+// Every mbarrier wait is bounded (globaltimer, Params::wait_ns): on expiry the CTA raises a
+// shared abort flag and a global status bit, drains its in-flight TMA, MMA and bulk copies
+// (bounded separately by Params::drain_ns), frees TMEM and returns.
+//
+// Built with FP8MQA_DEBUG_BOUNDS, every global access and TMA coordinate is checked first;
+// a violation is recorded in the status word and the access skipped.
 #pragma once
 
 #include <cstdint>
@@ -50,11 +53,7 @@ namespace fp8mqa {
 
 constexpr int kHeads = 32;
 constexpr int kDim = 128;
-// Query rows per unit (a multiple of 2, at most 8): kRows x 32 heads is the MMA N.
-#ifndef FP8MQA_ROWS
-#define FP8MQA_ROWS 8
-#endif
-constexpr int kRows = FP8MQA_ROWS;
+constexpr int kRows = 8;                  // query rows per unit: kRows x 32 heads is the MMA N
 constexpr int kTileKeys = 128;            // keys per tile (MMA M)
 constexpr int kUmmaN = kRows * kHeads;    // 256 (MMA N)
 constexpr int kUmmaK = 32;                // FP8 K per tcgen05.mma
@@ -65,15 +64,10 @@ constexpr int kClaimAhead = 4;           // K tiles of a unit left to issue when
 constexpr int kAccBufs = 2;
 constexpr uint32_t kAccStride = 256;      // TMEM columns between accumulator buffers
 constexpr uint32_t kTmemCols = kAccBufs * kAccStride;  // 512 (a power of two)
-// Query rows each epilogue warp reduces per tile (2 or 4): more rows per warp amortise the
-// per-tile synchronisation over more arithmetic, fewer rows give more warps per SM.
-#ifndef FP8MQA_ROWS_PER_WARP
-#define FP8MQA_ROWS_PER_WARP 2
-#endif
-constexpr int kRowsPerEpiWarp = FP8MQA_ROWS_PER_WARP;
+constexpr int kRowsPerEpiWarp = 2;
 constexpr int kEpiWarp0 = 4;
-constexpr int kEpiWarps = kRows * 4 / kRowsPerEpiWarp;  // 4 TMEM sub-partitions
-constexpr int kThreads = (kEpiWarp0 + kEpiWarps) * 32;
+constexpr int kEpiWarps = kRows * 4 / kRowsPerEpiWarp;  // 16: four TMEM sub-partitions
+constexpr int kThreads = (kEpiWarp0 + kEpiWarps) * 32;  // 640
 constexpr int kMmaWarp0 = 1;              // issues the even tiles (accumulator buffer 0)
 constexpr int kMmaWarp1 = 3;              // issues the odd tiles (accumulator buffer 1)
 constexpr int kFillWarp = 2;
@@ -114,22 +108,38 @@ constexpr uint32_t kOffMisc = kOffUnits + kUnitSlots * sizeof(UnitInfo);
 constexpr uint32_t kSmemUsed = kOffMisc + 16;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // slack for aligning the base
 static_assert(kSmemBytes <= 232448, "shared memory budget");
-static_assert(kRowsPerEpiWarp == 2 || kRowsPerEpiWarp == 4, "two or four rows per warp");
-static_assert(kRows % kRowsPerEpiWarp == 0 && kRows <= 8 && kUmmaN <= int(kAccStride),
-              "rows per unit");
+static_assert(kUmmaN <= int(kAccStride), "accumulator buffer width");
 static_assert(kQBytes % 1024 == 0 && kWBytes % 128 == 0, "shared-memory alignment");
 
 // Per-role register budgets (setmaxnreg): the control warpgroup gives registers to the
 // epilogue warpgroups; the total must stay within the launch allocation (threads x the
 // per-thread count the kernel is compiled to, which fills the register file).
-constexpr uint32_t kLaunchRegs = (65536u / kThreads) & ~7u;  // 168 or 96
-constexpr uint32_t kCtlRegs = kRowsPerEpiWarp == 4 ? 56u : 32u;
+constexpr uint32_t kLaunchRegs = (65536u / kThreads) & ~7u;  // 96
+constexpr uint32_t kCtlRegs = 32u;
 constexpr uint32_t kEpiRegs = ((kLaunchRegs * kThreads - 128u * kCtlRegs) / (kEpiWarps * 32u)) & ~7u;
 static_assert(128 * kCtlRegs + kEpiWarps * 32 * kEpiRegs <= kThreads * kLaunchRegs,
               "register split");
 
-// Status word bits.
+// Status word bits (status[0]); status[2..3] hold the first bounds violation (debug builds).
 constexpr int32_t kStatusTimeout = 1;
+constexpr int32_t kStatusBounds = 2;
+
+#ifdef FP8MQA_DEBUG_BOUNDS
+constexpr bool kDebugBounds = true;
+#else
+constexpr bool kDebugBounds = false;
+#endif
+
+// Kinds of bounds violation a debug build records.
+enum BoundsKind : uint32_t {
+    kBoundsStore = 1,     // epilogue logit store outside [0, M) x [0, N)
+    kBoundsKvScale = 2,   // kv_scale read outside [0, N)
+    kBoundsFill = 3,      // -inf span outside its row's [0, N)
+    kBoundsKTile = 4,     // K tile coordinate outside [0, ceil(N / 128))
+    kBoundsQBlock = 5,    // Q / w row block outside [0, M)
+    kBoundsWindow = 6,    // ks / ke read outside [0, M)
+    kBoundsTmem = 7,      // TMEM column outside the allocation
+};
 
 // Scheduler slot in global memory: work counters that the last CTA resets.
 struct SchedSlot {
@@ -153,9 +163,25 @@ struct Params {
     int32_t num_units;        // num_blocks * split
     int32_t clean;
     SchedSlot* sched;
-    int32_t* status;
-    uint64_t timeout_ns;
+    int32_t* status;          // status[0]: flags; status[2..3]: first bounds violation
+    uint64_t wait_ns;         // a pipeline wait gives up (abort) after this long
+    uint64_t drain_ns;        // bound of the waits for in-flight work before exit
+    uint32_t suspend_ns;      // 0: waits suspend for the hardware's own time; else at most this
 };
+
+// True when the access may go ahead: always in normal builds.  In debug builds, only when
+// `ok`; otherwise the first violation's (kind, index) goes to status[2..3] (the host's
+// check_error reports it) and kStatusBounds is set.
+__device__ __forceinline__ bool in_bounds(bool ok, int32_t* status, uint32_t kind, int64_t index)
+{
+    if (!kDebugBounds || ok) return true;
+    const unsigned long long v =
+        (static_cast<unsigned long long>(kind) << 48) |
+        (static_cast<unsigned long long>(index) & 0xFFFFFFFFFFFFull);
+    atomicCAS(reinterpret_cast<unsigned long long*>(status + 2), 0ull, v);
+    atomicOr(status, kStatusBounds);
+    return false;
+}
 
 // tcgen05 instruction descriptor: D f32, A = B = E4M3, both K-major, M = 128, N = 256.
 constexpr uint32_t kIdesc = (1u << 4)                          // D format: f32
@@ -186,24 +212,40 @@ struct IntTag {
     static constexpr int value = V;
 };
 
+// What a wait needs: the CTA's abort flag (shared memory) and the kernel parameters (read
+// from the constant bank only on a wait's slow path, so they hold no registers).
 struct Ctl {
     volatile int32_t* abort;
-    int32_t* status;
-    uint64_t timeout_ns;
+    const Params& p;
 };
 
-// Bounded single-thread wait.  Returns false when the CTA is aborting.
+// One poll of a wait's slow path.  By default try_wait suspends the thread in hardware until
+// the phase completes or a system-dependent time passes; a short wait limit also bounds the
+// suspension, so that the limit is checked in time.
+__device__ __forceinline__ bool poll_bar(uint32_t bar, uint32_t parity, const Ctl& c)
+{
+    return c.p.suspend_ns ? ptx::mbar_try_wait_sleep(bar, parity, c.p.suspend_ns)
+                          : ptx::mbar_try_wait(bar, parity);
+}
+
+__device__ __forceinline__ void raise_timeout(const Ctl& c)
+{
+    *c.abort = 1;
+    atomicOr(c.p.status, kStatusTimeout);
+}
+
+// Bounded single-thread wait.  try_wait suspends the thread in hardware for a while when the
+// phase is still open, so the loop issues few instructions.  Returns false when the CTA is
+// aborting or this wait ran out (which starts the abort).
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Ctl& c)
 {
     if (ptx::mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = ptx::globaltimer_ns();
     while (true) {
-        // sleep until the phase completes (or 20 us pass), then re-check abort and timeout
-        if (ptx::mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+        if (poll_bar(bar, parity, c)) return true;
         if (*c.abort) return false;
-        if (ptx::globaltimer_ns() - t0 > c.timeout_ns) {
-            *c.abort = 1;
-            atomicOr(c.status, kStatusTimeout);
+        if (ptx::globaltimer_ns() - t0 > c.p.wait_ns) {
+            raise_timeout(c);
             return false;
         }
     }
@@ -224,41 +266,30 @@ __device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity, con
     return ok != 0;
 }
 
-// Bounded wait by lane 0 only, result broadcast to the warp.  For barriers whose data the
-// warp reads through tcgen05 (ordered by tcgen05.fence::after_thread_sync), not through
-// generic loads.
-__device__ __forceinline__ bool wait_bar_lane0(uint32_t bar, uint32_t parity, const Ctl& c)
-{
-    int ok = 1;
-    if ((threadIdx.x & 31) == 0) ok = wait_bar(bar, parity, c) ? 1 : 0;
-    return __shfl_sync(0xffffffffu, ok, 0) != 0;
-}
-
-// Bounded wait by every lane of a warp, without lane-0 branches: all lanes poll and a warp
-// vote decides, so the warp stays converged.  Returns false (for the whole warp) when the
-// CTA is aborting or the wait timed out.
+// Bounded wait by every lane of a warp: all lanes poll and a warp vote decides, so the warp
+// stays converged.  Returns false (for the whole warp) when the CTA is aborting or the wait
+// ran out.
 __device__ __forceinline__ bool wait_bar_all(uint32_t bar, uint32_t parity, const Ctl& c)
 {
     if (__all_sync(0xffffffffu, ptx::mbar_try_wait(bar, parity))) return true;
     const uint64_t t0 = ptx::globaltimer_ns();
     while (true) {
-        if (__all_sync(0xffffffffu, ptx::mbar_try_wait_sleep(bar, parity, 20000u))) return true;
+        if (__all_sync(0xffffffffu, poll_bar(bar, parity, c))) return true;
         int stop = *c.abort ? 1 : 0;
-        if ((threadIdx.x & 31) == 0 && !stop && ptx::globaltimer_ns() - t0 > c.timeout_ns) {
-            *c.abort = 1;
-            atomicOr(c.status, kStatusTimeout);
+        if ((threadIdx.x & 31) == 0 && !stop && ptx::globaltimer_ns() - t0 > c.p.wait_ns) {
+            raise_timeout(c);
             stop = 1;
         }
         if (__any_sync(0xffffffffu, stop)) return false;
     }
 }
 
-// Drain: wait for a phase without looking at the abort flag (still time-bounded).
-__device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity, uint64_t timeout_ns)
+// Drain: wait for a phase without looking at the abort flag (bounded by drain_ns).
+__device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity, uint64_t drain_ns)
 {
     const uint64_t t0 = ptx::globaltimer_ns();
     while (!ptx::mbar_try_wait(bar, parity)) {
-        if (ptx::globaltimer_ns() - t0 > timeout_ns) break;
+        if (ptx::globaltimer_ns() - t0 > drain_ns) break;
     }
 }
 
@@ -287,13 +318,15 @@ __device__ __forceinline__ Geometry unit_geometry(const Params& p, int32_t b, in
     g.hi = 0;
     if (lane < kRows && g.m0 + lane < p.M) {
         const int64_t m = g.m0 + lane;
-        const int64_t s = clamp64(p.ks[m], 0, p.N);
-        const int64_t e = clamp64(p.ke[m], 0, p.N);
-        g.lo = int32_t(s);
-        g.hi = int32_t(e);
-        if (s < e) {
-            lo = s;
-            hi = e;
+        if (in_bounds(m >= 0 && m < p.M, p.status, kBoundsWindow, m)) {
+            const int64_t s = clamp64(p.ks[m], 0, p.N);
+            const int64_t e = clamp64(p.ke[m], 0, p.N);
+            g.lo = int32_t(s);
+            g.hi = int32_t(e);
+            if (s < e) {
+                lo = s;
+                hi = e;
+            }
         }
     }
 #pragma unroll
@@ -343,9 +376,14 @@ __device__ __forceinline__ Geometry unit_geometry(const Params& p, int32_t b, in
 // Warp-cooperative -inf fill of row[a, e): the 16-byte aligned middle goes out as bulk
 // copies (TMA engine) of up to kFillBytes from the shared-memory -inf buffer at `src`, issued
 // by lane 0; the ragged ends (under 4 floats each) are plain stores.
-__device__ __forceinline__ void fill_neg_inf(float* row, int64_t a, int64_t e, uint32_t src)
+__device__ __forceinline__ void fill_neg_inf(const Params& p, int64_t m, int64_t a, int64_t e,
+                                             uint32_t src)
 {
     if (a >= e) return;
+    if (!in_bounds(m >= 0 && m < p.M && a >= 0 && e <= p.N, p.status, kBoundsFill,
+                   m * p.N + (a < 0 || a >= p.N ? a : e)))
+        return;
+    float* row = p.out + m * p.N;
     const int lane = threadIdx.x & 31;
     const float ninf = __int_as_float(0xff800000u);
     const uintptr_t addr = reinterpret_cast<uintptr_t>(row + a);
@@ -363,101 +401,78 @@ __device__ __forceinline__ void fill_neg_inf(float* row, int64_t a, int64_t e, u
     }
 }
 
-__device__ __forceinline__ float2 relu2(uint32_t a, uint32_t b)
-{
-    return make_float2(fmaxf(__uint_as_float(a), 0.f), fmaxf(__uint_as_float(b), 0.f));
-}
-
 // Head quads (4 heads) whose relu runs on the FMA pipe instead of the ALU: for those the
-// sum takes s*w + |s|*w = 2 relu(s) w, in separate chains halved at the end.  Splitting the
-// relu between the ALU (max, half rate) and the FMA pipe (|x| operands are free) balances
-// the two pipes.  Any mask is valid; the default was chosen by measurement.
+// sum takes s*w + |s|*w = 2 relu(s) w, in a chain halved at the end.  Splitting the relu
+// between the ALU (max, half rate) and the FMA pipe (|x| operands are free) balances the
+// two pipes.  Any mask is valid; the default was chosen by measurement.
 #ifndef FP8MQA_ABS_QUADS
 #define FP8MQA_ABS_QUADS 0xA4u
 #endif
 constexpr uint32_t kAbsQuads = FP8MQA_ABS_QUADS;
 
 __device__ __forceinline__ float2 abs2(float2 v) { return make_float2(fabsf(v.x), fabsf(v.y)); }
+__device__ __forceinline__ float2 relu2(float2 v)
+{
+    return make_float2(fmaxf(v.x, 0.f), fmaxf(v.y, 0.f));
+}
+__device__ __forceinline__ float2 f2(uint32_t a, uint32_t b)
+{
+    return make_float2(__uint_as_float(a), __uint_as_float(b));
+}
 
 // sum_h relu(S[h]) * w[h] for two query rows: s[0..31] row a, s[32..63] row b; w of row a in
-// wsm[0..7] and of row b in wsm[8..15] (shared memory, 4 heads per float4).
+// wsm[0..7] and of row b in wsm[8..15] (shared memory, 4 heads per float4).  Two accumulator
+// chains per row (ALU-relu heads and FMA-relu heads), joined once at the end.
 __device__ __forceinline__ void relu_dot_2rows(const uint32_t (&s)[64], const float4* wsm,
                                                float& va, float& vb)
 {
-    constexpr bool kAnyMax = (kAbsQuads & 0xFFu) != 0xFFu;
-    constexpr bool kAnyAbs = (kAbsQuads & 0xFFu) != 0u;
-    float2 a[4], b[4], ca[2], cb[2];
-    bool a_init[4] = {false, false, false, false}, c_init = false;
+    float2 xa = make_float2(0.f, 0.f), xb = xa, ya = xa, yb = xa;  // x: ALU relu, y: FMA relu
+    bool x_init = false, y_init = false;
 #pragma unroll
     for (int j = 0; j < kHeads / 4; ++j) {
-        const float4 x = wsm[j];
-        const float4 y = wsm[kHeads / 4 + j];
-        const float2 wa0 = make_float2(x.x, x.y), wa1 = make_float2(x.z, x.w);
-        const float2 wb0 = make_float2(y.x, y.y), wb1 = make_float2(y.z, y.w);
-        const float2 sa0 = make_float2(__uint_as_float(s[4 * j]), __uint_as_float(s[4 * j + 1]));
-        const float2 sa1 = make_float2(__uint_as_float(s[4 * j + 2]), __uint_as_float(s[4 * j + 3]));
-        const float2 sb0 = make_float2(__uint_as_float(s[32 + 4 * j]), __uint_as_float(s[32 + 4 * j + 1]));
-        const float2 sb1 = make_float2(__uint_as_float(s[32 + 4 * j + 2]), __uint_as_float(s[32 + 4 * j + 3]));
+        const float4 u = wsm[j];
+        const float4 v = wsm[kHeads / 4 + j];
+        const float2 wa0 = make_float2(u.x, u.y), wa1 = make_float2(u.z, u.w);
+        const float2 wb0 = make_float2(v.x, v.y), wb1 = make_float2(v.z, v.w);
+        const float2 sa0 = f2(s[4 * j], s[4 * j + 1]), sa1 = f2(s[4 * j + 2], s[4 * j + 3]);
+        const float2 sb0 = f2(s[32 + 4 * j], s[32 + 4 * j + 1]);
+        const float2 sb1 = f2(s[32 + 4 * j + 2], s[32 + 4 * j + 3]);
         if (kAbsQuads & (1u << j)) {
-            if (!c_init) {
-                ca[0] = __fmul2_rn(sa0, wa0);
-                cb[0] = __fmul2_rn(sb0, wb0);
-                ca[1] = __fmul2_rn(sa1, wa1);
-                cb[1] = __fmul2_rn(sb1, wb1);
-                c_init = true;
+            if (!y_init) {
+                ya = __fmul2_rn(sa0, wa0);
+                yb = __fmul2_rn(sb0, wb0);
+                y_init = true;
             } else {
-                ca[0] = __ffma2_rn(sa0, wa0, ca[0]);
-                cb[0] = __ffma2_rn(sb0, wb0, cb[0]);
-                ca[1] = __ffma2_rn(sa1, wa1, ca[1]);
-                cb[1] = __ffma2_rn(sb1, wb1, cb[1]);
+                ya = __ffma2_rn(sa0, wa0, ya);
+                yb = __ffma2_rn(sb0, wb0, yb);
             }
-            ca[0] = __ffma2_rn(abs2(sa0), wa0, ca[0]);
-            cb[0] = __ffma2_rn(abs2(sb0), wb0, cb[0]);
-            ca[1] = __ffma2_rn(abs2(sa1), wa1, ca[1]);
-            cb[1] = __ffma2_rn(abs2(sb1), wb1, cb[1]);
+            ya = __ffma2_rn(abs2(sa0), wa0, ya);
+            yb = __ffma2_rn(abs2(sb0), wb0, yb);
+            ya = __ffma2_rn(sa1, wa1, ya);
+            yb = __ffma2_rn(sb1, wb1, yb);
+            ya = __ffma2_rn(abs2(sa1), wa1, ya);
+            yb = __ffma2_rn(abs2(sb1), wb1, yb);
         } else {
-            const int c = (2 * j) & 3;
-            const float2 ra0 = make_float2(fmaxf(sa0.x, 0.f), fmaxf(sa0.y, 0.f));
-            const float2 ra1 = make_float2(fmaxf(sa1.x, 0.f), fmaxf(sa1.y, 0.f));
-            const float2 rb0 = make_float2(fmaxf(sb0.x, 0.f), fmaxf(sb0.y, 0.f));
-            const float2 rb1 = make_float2(fmaxf(sb1.x, 0.f), fmaxf(sb1.y, 0.f));
-            if (!a_init[c]) {
-                a[c] = __fmul2_rn(ra0, wa0);
-                a[c + 1] = __fmul2_rn(ra1, wa1);
-                b[c] = __fmul2_rn(rb0, wb0);
-                b[c + 1] = __fmul2_rn(rb1, wb1);
-                a_init[c] = a_init[c + 1] = true;
+            if (!x_init) {
+                xa = __fmul2_rn(relu2(sa0), wa0);
+                xb = __fmul2_rn(relu2(sb0), wb0);
+                x_init = true;
             } else {
-                a[c] = __ffma2_rn(ra0, wa0, a[c]);
-                a[c + 1] = __ffma2_rn(ra1, wa1, a[c + 1]);
-                b[c] = __ffma2_rn(rb0, wb0, b[c]);
-                b[c + 1] = __ffma2_rn(rb1, wb1, b[c + 1]);
+                xa = __ffma2_rn(relu2(sa0), wa0, xa);
+                xb = __ffma2_rn(relu2(sb0), wb0, xb);
             }
+            xa = __ffma2_rn(relu2(sa1), wa1, xa);
+            xb = __ffma2_rn(relu2(sb1), wb1, xb);
         }
     }
-    float2 ra = make_float2(0.f, 0.f), rb = ra;
-    if (kAnyMax) {
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            if (a_init[c]) {
-                ra = __fadd2_rn(ra, a[c]);
-                rb = __fadd2_rn(rb, b[c]);
-            }
-        }
-    }
-    if (kAnyAbs) {
-        const float2 half = make_float2(0.5f, 0.5f);
-        ra = __ffma2_rn(__fadd2_rn(ca[0], ca[1]), half, ra);
-        rb = __ffma2_rn(__fadd2_rn(cb[0], cb[1]), half, rb);
+    const float2 half = make_float2(0.5f, 0.5f);
+    float2 ra = xa, rb = xb;
+    if (y_init) {
+        ra = x_init ? __ffma2_rn(ya, half, xa) : __fmul2_rn(ya, half);
+        rb = x_init ? __ffma2_rn(yb, half, xb) : __fmul2_rn(yb, half);
     }
     va = ra.x + ra.y;
     vb = rb.x + rb.y;
-}
-
-__device__ __forceinline__ float sum4(const float2 (&a)[4])
-{
-    const float2 r = __fadd2_rn(__fadd2_rn(a[0], a[1]), __fadd2_rn(a[2], a[3]));
-    return r.x + r.y;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -471,14 +486,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* smem = smem_raw + pad;
     const uint32_t sbase = raw_base + pad;
 
-    const int warp = threadIdx.x >> 5;
+    // warp-uniform role index (the shuffle tells the compiler it is uniform, so addresses
+    // derived from it can live in uniform registers)
+    const int warp = __shfl_sync(0xffffffffu, int(threadIdx.x >> 5), 0);
     const int lane = threadIdx.x & 31;
 
     auto bar = [&](int i) -> uint32_t { return sbase + kOffBar + 8u * uint32_t(i); };
     UnitInfo* units = reinterpret_cast<UnitInfo*>(smem + kOffUnits);
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + kOffMisc);
     volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(smem + kOffMisc + 4);
-    const Ctl ctl{abort_flag, p.status, p.timeout_ns};
+    const Ctl ctl{abort_flag, p};
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
@@ -513,7 +530,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
-    const uint32_t tmem_base = *tmem_slot;
+    const uint32_t tmem_base = __shfl_sync(0xffffffffu, *tmem_slot, 0);
 
     if (warp < kEpiWarp0) ptx::regs_dec<kCtlRegs>();
 
@@ -576,10 +593,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = wait_bar(bar(kBarQEmpty + qs), ((qi / kQSlots) & 1u) ^ 1u, ctl);
                     if (ok) {
                         const uint32_t fb = bar(kBarQFull + qs);
-                        ptx::mbar_arrive_expect_tx(fb, kQBytes + kWBytes);
-                        ptx::tma_load_2d_hint(sbase + kOffQ + qs * kQBytes, &tm_q, fb, 0,
-                                              geo.m0 * kHeads, pol_q);
-                        ptx::tma_load_2d(sbase + kOffW + qs * kWBytes, &tm_w, fb, 0, geo.m0);
+                        if (in_bounds(geo.m0 >= 0 && geo.m0 < p.M, p.status, kBoundsQBlock,
+                                      geo.m0)) {
+                            ptx::mbar_arrive_expect_tx(fb, kQBytes + kWBytes);
+                            ptx::tma_load_2d_hint(sbase + kOffQ + qs * kQBytes, &tm_q, fb, 0,
+                                                  geo.m0 * kHeads, pol_q);
+                            ptx::tma_load_2d(sbase + kOffW + qs * kWBytes, &tm_w, fb, 0,
+                                             geo.m0);
+                        } else {
+                            ptx::mbar_arrive(fb);
+                        }
                         ++qi;
                     }
                 }
@@ -610,9 +633,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     issued = wait_bar(bar(kBarKEmpty + st), ((g / kStages) & 1u) ^ 1u, ctl) ? 1 : 0;
                     if (issued) {
                         const uint32_t fb = bar(kBarKFull + st);
-                        ptx::mbar_arrive_expect_tx(fb, kKBytes);
-                        ptx::tma_load_2d_hint(sbase + kOffK + st * kKBytes, &tm_k, fb, 0,
-                                              t * kTileKeys, pol_k);
+                        if (in_bounds(t >= 0 && t < p.num_tiles, p.status, kBoundsKTile, t)) {
+                            ptx::mbar_arrive_expect_tx(fb, kKBytes);
+                            ptx::tma_load_2d_hint(sbase + kOffK + st * kKBytes, &tm_k, fb, 0,
+                                                  t * kTileKeys, pol_k);
+                        } else {
+                            ptx::mbar_arrive(fb);
+                        }
                     }
                 }
                 ok = __shfl_sync(0xffffffffu, issued, 0) != 0;
@@ -628,9 +655,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             // Wait for any TMA load still in flight before the CTA can exit: only the last
             // kStages K loads and the last kQSlots Q loads can be outstanding.
             for (uint32_t j = (g > kStages ? g - kStages : 0); j < g; ++j)
-                drain_bar(bar(kBarKFull + j % kStages), (j / kStages) & 1u, p.timeout_ns);
+                drain_bar(bar(kBarKFull + j % kStages), (j / kStages) & 1u, p.drain_ns);
             for (uint32_t j = (qi > kQSlots ? qi - kQSlots : 0); j < qi; ++j)
-                drain_bar(bar(kBarQFull + j % kQSlots), (j / kQSlots) & 1u, p.timeout_ns);
+                drain_bar(bar(kBarQFull + j % kQSlots), (j / kQSlots) & 1u, p.drain_ns);
         }
     } else if (warp == kMmaWarp0 || warp == kMmaWarp1) {
         // ------------------------------------------------------------ MMA issuers
@@ -686,7 +713,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // all MMAs issued by this thread complete before TMEM can be released
             ptx::mma_commit(bar(kBarDrain));
-            drain_bar(bar(kBarDrain), 0, p.timeout_ns);
+            drain_bar(bar(kBarDrain), 0, p.drain_ns);
         }
         __syncwarp();
     } else if (warp < kEpiWarp0) {
@@ -722,9 +749,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int r = 0; r < kRows; ++r) {
                     const int64_t m = int64_t(geo.m0) + r;
                     if (m >= p.M) break;
-                    float* row = p.out + m * p.N;
-                    fill_neg_inf(row, col_lo, left_end, src);
-                    fill_neg_inf(row, right_beg, col_hi, src);
+                    fill_neg_inf(p, m, col_lo, left_end, src);
+                    fill_neg_inf(p, m, right_beg, col_hi, src);
                 }
                 if (lane == 0) {
                     // keep at most a few units' bulk copies queued
@@ -740,12 +766,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ------------------------------------------------------------ epilogue
         ptx::regs_inc<kEpiRegs>();
-        constexpr int kPairs = kRowsPerEpiWarp / 2;
         const int sp = warp & 3;                                // TMEM sub-partition
-        const int grp = (warp - kEpiWarp0) >> 2;               // which rows of the 8
-        const uint32_t lane_base = uint32_t(sp * 32) << 16;
+        const int grp = (warp - kEpiWarp0) >> 2;               // rows 2 grp, 2 grp + 1 of the 8
+        const uint32_t tcol = uint32_t(grp * kRowsPerEpiWarp * kHeads);
+        const uint32_t tm_warp = tmem_base + (uint32_t(sp * 32) << 16) + tcol;
+        const uint32_t full0 = bar(kBarAccFull), empty0 = bar(kBarAccEmpty);
         const float ninf = __int_as_float(0xff800000u);
-        const int32_t N = int32_t(p.N);
+        if (!in_bounds(tcol + kAccStride + kRowsPerEpiWarp * kHeads <= kTmemCols, p.status,
+                       kBoundsTmem, tcol))
+            ctl.abort[0] = 1;
         uint32_t ui = 0, g = 0, qi = 0;
         bool ok = true;
         while (ok) {
@@ -754,12 +783,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the unit and this warp's rows' windows, copied out before the slot is released
             const UnitInfo& src = units[slot];
             const int32_t flags = src.flags, m0 = src.m0, t0 = src.t0, t1 = src.t1;
-            int32_t lo[kRowsPerEpiWarp], hi[kRowsPerEpiWarp];
-#pragma unroll
-            for (int r = 0; r < kRowsPerEpiWarp; ++r) {
-                lo[r] = src.lo[grp * kRowsPerEpiWarp + r];
-                hi[r] = src.hi[grp * kRowsPerEpiWarp + r];
-            }
+            const int32_t lo_a = src.lo[2 * grp], hi_a = src.hi[2 * grp];
+            const int32_t lo_b = src.lo[2 * grp + 1], hi_b = src.hi[2 * grp + 1];
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(bar(kBarUnitEmpty + slot));
             ++ui;
@@ -773,100 +798,88 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float4* wsm = reinterpret_cast<const float4*>(
                 smem + kOffW + qs * kWBytes + grp * kRowsPerEpiWarp * kHeads * 4);
 
-            // This warp's rows: output rows, and the key tiles that lie inside every row's
-            // window (stored without compare/select).
-            const int64_t m_first = int64_t(m0) + grp * kRowsPerEpiWarp;
-            bool rok[kRowsPerEpiWarp];
-            int32_t tcl = 0, tch = INT32_MAX;
-#pragma unroll
-            for (int r = 0; r < kRowsPerEpiWarp; ++r) {
-                rok[r] = m_first + r < p.M;
-                tcl = max(tcl, (lo[r] + kTileKeys - 1) / kTileKeys);
-                tch = min(tch, hi[r] / kTileKeys);
-            }
-            if (!rok[kRowsPerEpiWarp - 1]) tch = 0;  // rows past M take the masked path
-            float* row0 = p.out + m_first * p.N;
+            // This warp's rows, and the key tiles that lie inside both rows' windows (stored
+            // without compare/select).  Rows past M have empty windows.
+            const int64_t ma = int64_t(m0) + 2 * grp;
+            const bool ok_a = ma < p.M, ok_b = ma + 1 < p.M;
+            int32_t cs = max((lo_a + kTileKeys - 1) / kTileKeys, (lo_b + kTileKeys - 1) / kTileKeys);
+            int32_t ce = min(hi_a / kTileKeys, hi_b / kTileKeys);
+            if (!ok_b) ce = 0;
+            cs = max(t0, min(cs, t1));
+            ce = max(cs, min(ce, t1));
 
-            // Per-tile state: accumulator buffer ab = g & 1 selects the barrier and the TMEM
-            // column half, the barrier parity ph flips after every buffer-1 tile.
-            const uint32_t full0 = bar(kBarAccFull), empty0 = bar(kBarAccEmpty);
-            const uint32_t tm0 = tmem_base + lane_base + uint32_t(grp * kRowsPerEpiWarp * kHeads);
-            uint32_t ph = (g >> 1) & 1u;
+            // this lane's key, and its rows' starts (row b's is row a's plus N, formed per tile:
+            // fewer live registers than two running pointers)
             int32_t n = t0 * kTileKeys + sp * 32 + lane;
-            float* op[kRowsPerEpiWarp];  // this lane's output element in each of the warp's rows
-#pragma unroll
-            for (int r = 0; r < kRowsPerEpiWarp; ++r) op[r] = row0 + r * p.N + n;
-            const float* const kvp = p.kv_scale;
-            const int32_t n_last = N - 1;
-            const bool clean_out = p.clean != 0;
+            float* const row_a = p.out + (ok_a ? ma : 0) * p.N;
+            uint32_t ph = (g >> 1) & 1u;
             // kv_scale one tile ahead; past the end the index is clamped (the value is unused)
-            float kv_next = __ldg(kvp + min(n, n_last));
+            float kv_next = __ldg(p.kv_scale + min(n, int32_t(p.N) - 1));
 
-            // One tile.  kClean: the tile lies inside every row's window (no compare/select).
-            // kAB: the accumulator buffer when known at compile time (the clean middle runs in
-            // buffer pairs), -1 when it comes from the tile count.
-            auto step = [&](auto clean_tag, auto ab_tag) -> bool {
+            // One tile.  kClean: inside both rows' windows (no compare/select).  kAB: the
+            // accumulator buffer when known at compile time (the clean middle runs in buffer
+            // pairs), -1 when it comes from the tile count.
+            auto tile = [&](auto clean_tag, auto ab_tag) -> bool {
                 constexpr bool kClean = decltype(clean_tag)::value;
                 constexpr int kAB = decltype(ab_tag)::value;
                 const uint32_t ab = kAB >= 0 ? uint32_t(kAB) : (g & 1u);
-                const float kv = kv_next;
-                kv_next = __ldg(kvp + min(n + kTileKeys, n_last));
                 if (!wait_bar_all(full0 + 8u * ab, ph, ctl)) return false;
                 ptx::tc_fence_after();
-                const uint32_t taddr = tm0 + ab * kAccStride;
-                // Copy all of this warp's accumulators out of TMEM and release the buffer at
-                // once, so the MMA can refill it while this warp does the arithmetic.
-                float v[kRowsPerEpiWarp];
-                {
-                    uint32_t s[kPairs][64];
-#pragma unroll
-                    for (int pp = 0; pp < kPairs; ++pp)
-                        ptx::tmem_ld_32x32b_x64_sync(taddr + uint32_t(pp * 2 * kHeads), s[pp]);
-                    ptx::tc_fence_before();
-                    ptx::mbar_arrive(empty0 + 8u * ab);  // all 32 lanes arrive
-#pragma unroll
-                    for (int pp = 0; pp < kPairs; ++pp)
-                        relu_dot_2rows(s[pp], wsm + pp * 2 * (kHeads / 4), v[2 * pp], v[2 * pp + 1]);
-                }
+                // Copy this warp's accumulators out of TMEM and release the buffer at once,
+                // so the MMA can refill it while this warp does the arithmetic.
+                uint32_t s[64];
+                ptx::tmem_ld_32x32b_x64_sync(tm_warp + ab * kAccStride, s);
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(empty0 + 8u * ab);  // all 32 lanes arrive
+                const float kv = kv_next;
+                const int32_t n_kv = min(n + kTileKeys, int32_t(p.N) - 1);
+                if (in_bounds(n_kv >= 0 && n_kv < p.N, p.status, kBoundsKvScale, n_kv))
+                    kv_next = __ldg(p.kv_scale + n_kv);
+                float va, vb;
+                relu_dot_2rows(s, wsm, va, vb);
+                float* const pa = row_a + n;
+                float* const pb = pa + p.N;
                 if (kClean) {
-                    // inside every row's window, so n < N and all rows exist
-#pragma unroll
-                    for (int r = 0; r < kRowsPerEpiWarp; ++r) __stcs(op[r], v[r] * kv);
-                } else if (n < N) {
-#pragma unroll
-                    for (int r = 0; r < kRowsPerEpiWarp; ++r) {
-                        if (!rok[r]) continue;
-                        if (n >= lo[r] && n < hi[r])
-                            __stcs(op[r], v[r] * kv);
-                        else if (clean_out)
-                            __stcs(op[r], ninf);
+                    // inside both rows' windows, so n < N and both rows exist
+                    if (in_bounds(n < p.N && ok_b, p.status, kBoundsStore, n)) {
+                        __stcs(pa, va * kv);
+                        __stcs(pb, vb * kv);
+                    }
+                } else if (n < p.N) {
+                    if (ok_a && in_bounds(ma < p.M, p.status, kBoundsStore, n)) {
+                        if (n >= lo_a && n < hi_a)
+                            __stcs(pa, va * kv);
+                        else if (p.clean)
+                            __stcs(pa, ninf);
+                    }
+                    if (ok_b && in_bounds(ma + 1 < p.M, p.status, kBoundsStore, n)) {
+                        if (n >= lo_b && n < hi_b)
+                            __stcs(pb, vb * kv);
+                        else if (p.clean)
+                            __stcs(pb, ninf);
                     }
                 }
                 n += kTileKeys;
-#pragma unroll
-                for (int r = 0; r < kRowsPerEpiWarp; ++r) op[r] += kTileKeys;
                 ph ^= ab;
                 ++g;
                 return true;
             };
             // masked head, clean middle (in buffer pairs), masked tail
-            const int32_t cs = max(t0, min(tcl, t1));
-            const int32_t ce = max(cs, min(tch, t1));
             int32_t t = t0;
-            for (; ok && t < cs; ++t) ok = step(BoolTag<false>{}, IntTag<-1>{});
+            for (; ok && t < cs; ++t) ok = tile(BoolTag<false>{}, IntTag<-1>{});
             if (ok && t < ce && (g & 1u)) {
-                ok = step(BoolTag<true>{}, IntTag<-1>{});
+                ok = tile(BoolTag<true>{}, IntTag<-1>{});
                 ++t;
             }
             for (; ok && t + 1 < ce; t += 2) {
-                ok = step(BoolTag<true>{}, IntTag<0>{});
-                if (ok) ok = step(BoolTag<true>{}, IntTag<1>{});
+                ok = tile(BoolTag<true>{}, IntTag<0>{});
+                if (ok) ok = tile(BoolTag<true>{}, IntTag<1>{});
             }
             if (ok && t < ce) {
-                ok = step(BoolTag<true>{}, IntTag<-1>{});
+                ok = tile(BoolTag<true>{}, IntTag<-1>{});
                 ++t;
             }
-            for (; ok && t < t1; ++t) ok = step(BoolTag<false>{}, IntTag<-1>{});
+            for (; ok && t < t1; ++t) ok = tile(BoolTag<false>{}, IntTag<-1>{});
             if (!ok) break;
             // this warp is done with the unit's w
             __syncwarp();

@@ -19,10 +19,19 @@
  *   - Return value: FP8MQA_OK (0) or a negative fp8mqa_status.  Argument errors are
  *     detected on the host BEFORE anything is enqueued; the library never aborts or
  *     exits the process and throws no exceptions.
- *   - The library keeps one small device buffer per device (a scheduler slot ring and a
- *     status word, under 1 KB), allocated on the first compute call on that device and
+ *   - The library keeps one small device buffer per device (about 260 KB: scheduler
+ *     slots and a status word), allocated on the first compute call on that device and
  *     kept until process exit.  That first call therefore must not be made while the
  *     stream is being captured into a CUDA graph.
+ *   - Scheduler slots.  Each launch's work queue lives in a slot of that buffer.  Direct
+ *     launches take slots from a ring of 256 in turn, so more than 256 launches running
+ *     at the same moment (on many streams) would share slots and produce wrong output.
+ *     A launch made while its stream is being captured into a CUDA graph gets a slot of
+ *     its own that no other launch ever uses (a graph's kernel keeps its slot for every
+ *     replay); up to 16384 launches can be captured per device and process, after which
+ *     capturing returns FP8MQA_ERR_CAPACITY.  Replays of one instantiated graph are
+ *     ordered by CUDA; two instantiations of the same captured graph must not run at
+ *     the same time.
  */
 #ifndef FP8_MQA_LOGITS_H
 #define FP8_MQA_LOGITS_H
@@ -48,7 +57,9 @@ enum fp8mqa_status {
     FP8MQA_ERR_ARCH = -4,              /* current device is not compute capability 10.3     */
     FP8MQA_ERR_LAUNCH = -5,            /* the kernel could not be configured or launched    */
     FP8MQA_ERR_TIMEOUT = -6,           /* a bounded on-device wait gave up (see check_error) */
-    FP8MQA_ERR_CUDA = -7               /* a CUDA runtime call failed                        */
+    FP8MQA_ERR_CUDA = -7,              /* a CUDA runtime call failed                        */
+    FP8MQA_ERR_BOUNDS = -8,            /* a bounds-checking build found a bad access        */
+    FP8MQA_ERR_CAPACITY = -9           /* no scheduler slot left for another captured launch */
 };
 
 /*
@@ -88,11 +99,14 @@ FP8MQA_API int fp8_mqa_logits(const uint8_t* q_fp8, const uint8_t* k_fp8, const 
 
 /*
  * fp8_mqa_logits_is_supported -- 1 if (M, N, H, D) is inside this library's contract
- * (H = 32, D = 128, M >= 0, N >= 0, M*H < 2^31, N < 2^31), else 0.  Pure host
- * arithmetic: it touches no device and may be called without a GPU (the page's
- * is_supported(), section "Motivation").
+ * (H = 32, D = 128, M >= 0, N >= 0, M*H < 2^31, N < 2^31) and, for device >= 0, CUDA
+ * device `device` exists and has compute capability 10.3; else 0 (the page's
+ * is_supported(), section "Motivation").  With device < 0 it is pure host arithmetic and
+ * may be called without a GPU; with device >= 0 it only queries device attributes (it
+ * launches and allocates nothing).
  */
-FP8MQA_API int fp8_mqa_logits_is_supported(int64_t M, int64_t N, int32_t H, int32_t D);
+FP8MQA_API int fp8_mqa_logits_is_supported(int64_t M, int64_t N, int32_t H, int32_t D,
+                                           int32_t device);
 
 /*
  * fp8_mqa_logits_default_split -- the split_n that split_n = 0 selects for an
@@ -102,11 +116,25 @@ FP8MQA_API int fp8_mqa_logits_default_split(int64_t M, int64_t N, int32_t num_sm
 
 /*
  * fp8_mqa_logits_check_error -- synchronizes `stream`, then reads and clears the
- * current device's status word.  Returns FP8MQA_ERR_TIMEOUT if any launch since the
- * last check had a bounded on-device wait give up (its output is then incomplete),
- * FP8MQA_ERR_CUDA if the synchronization itself failed, else FP8MQA_OK.
+ * current device's status words: the one of fp8_mqa_logits / fp8_mqa_logits_host and the
+ * one of fp8_mqa_logits_noalloc (each only if a call has set it up; this call allocates
+ * nothing).  Returns FP8MQA_ERR_TIMEOUT if a launch since the last check had a bounded
+ * on-device wait give up (its output is then incomplete), FP8MQA_ERR_BOUNDS if a
+ * bounds-checking build of the library recorded an out-of-range access,
+ * FP8MQA_ERR_CUDA if the synchronization or a read failed, else FP8MQA_OK.
  */
 FP8MQA_API int fp8_mqa_logits_check_error(void* stream);
+
+/*
+ * fp8_mqa_logits_set_wait_limit_ns -- sets how long one on-device pipeline wait may last
+ * before the kernel gives up (FP8MQA_ERR_TIMEOUT, reported by check_error), for launches
+ * enqueued after the call; 0 restores the default of 1 s.  Returns the previous limit.
+ * A kernel that gives up still waits for its own copies and tensor-core work in flight
+ * (for up to 1 s more) before it frees its resources and exits; the next launch is
+ * unaffected.  Meant for diagnostics and for testing that failure path; a limit far
+ * below a call's duration makes every call fail.  Host only; process-wide.
+ */
+FP8MQA_API uint64_t fp8_mqa_logits_set_wait_limit_ns(uint64_t ns);
 
 /*
  * fp8_mqa_logits_host_workspace_bytes -- size of the device workspace that
@@ -163,8 +191,8 @@ FP8MQA_API int fp8_mqa_logits_host(const uint8_t* q_fp8, const uint8_t* k_fp8, c
  *     before its kernel, so calls that overlap on the GPU (for example on two streams
  *     at once) race on them and may produce wrong output: order such calls on one
  *     stream or with events.
- *   - A bounded on-device wait that gives up is recorded in the array's status word,
- *     which fp8_mqa_logits_check_error does not read.
+ *   - A bounded on-device wait that gives up is recorded in the array's status word;
+ *     fp8_mqa_logits_check_error reads and clears it (and allocates nothing).
  */
 FP8MQA_API int fp8_mqa_logits_noalloc(const uint8_t* q_fp8, const uint8_t* k_fp8,
                                       const float* kv_scale, const float* w, const int32_t* ks,

@@ -79,3 +79,21 @@ def assert_parity(gpu, ref, inside, clean, extra_tol=None, what=""):
     assert np.all(err <= tol), (f"{what}: {int((err > tol).sum())} in-window values out of "
                                 f"tolerance; worst |err|={err.flat[worst]:.3e} "
                                 f"tol={tol.flat[worst]:.3e} ref={r.flat[worst]:.6g}")
+
+
+def assert_parity_full(outputs, inp, block_rows=256, what=""):
+    """Every entry of full-size GPU outputs against the oracle.
+
+    outputs: list of (label, float32 [M, N] host array, clean) for one workload's inputs.
+    The oracle runs once, in blocks of ``block_rows`` rows (bounded host memory), and every
+    output is compared element by element with each block: the mask bit-exact (-inf with
+    clean_logits=1, the untouched poison with 0) and every in-window value within the
+    tolerance."""
+    M, N = inp["M"], inp["N"]
+    for r0 in range(0, M, block_rows):
+        rows = np.arange(r0, min(M, r0 + block_rows), dtype=np.int64)
+        ref = run_oracle(inp, clean=True, rows=rows)
+        inside = window_mask(inp["ks"], inp["ke"], N, rows)
+        for label, gpu, clean in outputs:
+            assert_parity(gpu[r0:r0 + len(rows)], ref, inside, clean,
+                          what=f"{what} {label} rows {r0}..{r0 + len(rows) - 1}")

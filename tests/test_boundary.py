@@ -16,7 +16,7 @@ OK, INVALID, UNSUPPORTED, MISALIGNED = 0, -1, -2, -3
 
 @pytest.fixture(scope="module")
 def lib():
-    fm.build()
+    fm.build()  # the library and its bounds-checking variant
     return fm.lib()
 
 
@@ -32,8 +32,9 @@ def test_header_declares_expected_entry_points():
     assert set(names) == set(fm.SIGNATURES)
 
 
-def test_library_exports_every_declared_symbol(lib):
-    handle = ctypes.CDLL(fm.LIB_PATH)
+@pytest.mark.parametrize("path", [fm.LIB_PATH, fm.DEBUG_LIB_PATH])
+def test_library_exports_every_declared_symbol(lib, path):
+    handle = ctypes.CDLL(path)
     for name in header_functions():
         assert hasattr(handle, name), name
 
@@ -57,6 +58,10 @@ def test_is_supported_truth_table(lib):
     assert not fm.is_supported(2 ** 26, 16)       # M*H = 2^31
     assert fm.is_supported(2 ** 26 - 1, 16)
     assert not fm.is_supported(16, 2 ** 31)
+    # a device index that does not exist (or, here, no GPU at all) is never supported; a
+    # negative index skips the device check
+    assert not fm.is_supported(16, 16, device=4096)
+    assert fm.is_supported(16, 16, device=-1)
 
 
 def test_default_split(lib):
@@ -108,6 +113,16 @@ def test_rejects_before_any_device_work(lib):
     # empty problems are a no-op that never touches the device, even with null pointers
     assert _call(lib, M=0, ptrs=[None] * 7) == OK
     assert _call(lib, N=0, ptrs=[None] * 7) == OK
+
+
+def test_wait_limit_setter_round_trips(lib):
+    prev = fm.set_wait_limit_ns(12345)
+    try:
+        assert prev == 10 ** 9                      # the default: one second
+        assert fm.set_wait_limit_ns(0) == 12345     # 0 restores the default
+        assert fm.set_wait_limit_ns(0) == 10 ** 9
+    finally:
+        fm.set_wait_limit_ns(0)
 
 
 def test_host_entry_rejects_bad_workspace(lib):

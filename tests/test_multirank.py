@@ -48,3 +48,37 @@ def test_max_over_ranks_single_process():
     sys.path.insert(0, ROOT)
     import bench
     assert bench.max_over_ranks(3.5, 1) == 3.5
+
+
+def test_replica_command_starts_one_rank_per_gpu():
+    sys.path.insert(0, ROOT)
+    import bench
+    cmd = bench.replica_command(4, ["--steps", "7", "--gpus", "4"], port=29555)
+    assert cmd[1:3] == ["-m", "torch.distributed.run"]
+    assert "--nproc-per-node=4" in cmd and "--master-addr=127.0.0.1" in cmd
+    assert "--master-port=29555" in cmd
+    assert cmd[-4:] == ["--steps", "7", "--gpus", "4"]
+    assert cmd[-5].endswith("bench.py")
+
+
+def test_gpus_must_match_world_size(monkeypatch):
+    sys.path.insert(0, ROOT)
+    import bench
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    with pytest.raises(SystemExit, match="WORLD_SIZE=2"):
+        bench.main(["--gpus", "4"])
+    monkeypatch.delenv("WORLD_SIZE")
+    with pytest.raises(SystemExit, match="at least 1"):
+        bench.main(["--gpus", "0"])
+
+
+def test_algorithmic_bytes_and_flops():
+    sys.path.insert(0, ROOT)
+    import bench
+    import workloads
+    inp = workloads.make(workloads.WORKLOADS["tiny_causal_64x256"])
+    pairs = workloads.valid_pairs(inp["ks"], inp["ke"], inp["N"])
+    assert bench.valid_flops(inp) == 2 * 32 * 128 * pairs
+    inputs = 64 * 32 * 128 + 64 * 32 * 4 + 256 * 132 + 8 * 64
+    assert bench.algorithmic_bytes(inp, 1) == 4 * 64 * 256 + inputs
+    assert bench.algorithmic_bytes(inp, 0) == 4 * pairs + inputs

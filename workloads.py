@@ -53,6 +53,15 @@ WORKLOADS = {
     # under the context-parallel window family of the page's op test.
     "kpool_causal_16384x32000": Workload("kpool_causal_16384x32000", 16384, 32000, "causal", 5),
     "cp_4096x32768": Workload("cp_4096x32768", 4096, 32768, "cp", 6),
+    # The table's remaining rows: the causal 2048 x 65536 chunk and the multi-request
+    # block (4 requests each) at 2048 x 65536, 1024 x 131072 and 8192 x 8192.
+    "chunk_causal_2048x65536": Workload("chunk_causal_2048x65536", 2048, 65536, "causal", 7),
+    "multi_req_2048x65536": Workload("multi_req_2048x65536", 2048, 65536, "multi_req", 8,
+                                     requests=4),
+    "multi_req_1024x131072": Workload("multi_req_1024x131072", 1024, 131072, "multi_req", 9,
+                                      requests=4),
+    "multi_req_8192x8192": Workload("multi_req_8192x8192", 8192, 8192, "multi_req", 10,
+                                    requests=4),
 }
 
 WINDOW_FAMILIES = ("causal", "cp", "misaligned", "empty", "past_end", "multi_req")
@@ -105,6 +114,23 @@ def windows(family: str, M: int, N: int, requests: int = 4):
     else:
         raise ValueError(f"unknown window family {family!r}")
     return ks.astype(np.int32), ke.astype(np.int32)
+
+
+def describe(wl: Workload) -> str:
+    """One-line statement of a workload's windows, for reports."""
+    M, N = wl.M, wl.N
+    if wl.windows == "causal":
+        return f"causal: ks=0, ke={N - M}+m+1"
+    if wl.windows == "multi_req":
+        S, R = N // wl.requests, M // wl.requests
+        return (f"multi_req: {wl.requests} requests; request r=m//{R}, row i=m%{R}: "
+                f"ks={S}r, ke={S}r+{S - R}+i+1")
+    if wl.windows == "cp":
+        half = M // 2
+        off0 = max(0, (N - M) // 3 + 5)
+        return (f"cp: ks=0; rows m<{half}: ke={off0}+m+1, rows m>={half}: "
+                f"ke={N - (M - half)}+(m-{half})+1")
+    return wl.windows
 
 
 def draw(M: int, N: int, seed: int, H: int = H_DEFAULT, D: int = D_DEFAULT):
