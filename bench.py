@@ -495,6 +495,44 @@ def run_topk(args):
     return 0
 
 
+def run_split_sweep(args):
+    """Time the workload at each explicit split_n of --sweep-split and at the default
+    (split_n = 0): one JSON line with the table and the default's distance from the best."""
+    import torch
+
+    import fp8_mqa_logits_02_gb300 as fm
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    fm.lib()
+    sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
+    wl = workloads.WORKLOADS[args.workload]
+    inp = workloads.make(wl)
+    args_dev = _device_inputs(inp, dev)
+    out = torch.empty((inp["M"], inp["N"]), dtype=torch.float32, device=dev)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    flops = valid_flops(inp)
+    default = fm.default_split(inp["M"], inp["N"], sm_count)
+    table = []
+    for split_n in [0] + [int(x) for x in args.sweep_split.split(",")]:
+        ms, clocks = time_calls(fm, args_dev, out, args.clean, split_n, args.steps,
+                                args.warmup, flush, stream, dev)
+        us = statistics.mean(ms) * 1e3
+        table.append({"split_n": split_n, "split_used": split_n or default, "us_per_call": us,
+                      "tflops": flops / us / 1e6,
+                      "sm_mhz": clocks["sm_mhz"] if clocks else None})
+    best = min(table[1:], key=lambda r: r["us_per_call"])
+    print(json.dumps({
+        "metric": "split_n sweep, µs per call", "workload": wl.name,
+        "windows": workloads.describe(wl), "clean_logits": args.clean, "steps": args.steps,
+        "default_split": default, "default_us": table[0]["us_per_call"],
+        "best_explicit": best["split_n"], "best_us": best["us_per_call"],
+        "default_over_best": table[0]["us_per_call"] / best["us_per_call"],
+        "table": table}), flush=True)
+    return 0
+
+
 # Revision tag of the kernel the committed ncu traffic figure was taken on.
 KERNEL_REV = "v6"
 
@@ -513,6 +551,8 @@ def parse_args(argv=None):
                     help="skip the per-workload block (the headline call only)")
     ap.add_argument("--topk", type=int, default=0,
                     help="time the per-row top-k (this k) over the workload's logits instead")
+    ap.add_argument("--sweep-split", default="",
+                    help="comma-separated split_n values: time each (and the default) instead")
     ap.add_argument("--reference-rows", type=int, default=4096,
                     help="query rows of the workload the CPU-baseline sample computes")
     args = ap.parse_args(argv)
@@ -537,6 +577,8 @@ def main(argv=None):
         return run_reference(args)
     if args.topk:
         return run_topk(args)
+    if args.sweep_split:
+        return run_split_sweep(args)
     return run_gpu(args)
 
 

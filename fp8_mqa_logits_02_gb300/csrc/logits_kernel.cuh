@@ -517,11 +517,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mbar_init(bar(kBarDrain), 2);
         *abort_flag = 0;
         ptx::mbar_init_fence();
-    }
-    if (warp == 0 && lane == 0) {
+        // Each CTA's first unit is its own index (no shared counter): its Q + w load starts
+        // now, before the set-up barrier, and overlaps the reads of the unit's windows.
         ptx::prefetch_tensormap(&tm_q);
-        ptx::prefetch_tensormap(&tm_k);
         ptx::prefetch_tensormap(&tm_w);
+        const int32_t b0 = p.num_blocks - 1 - int32_t(blockIdx.x / uint32_t(p.split));
+        if (in_bounds(b0 >= 0 && int64_t(b0) * kRows < p.M, p.status, kBoundsQBlock, b0)) {
+            ptx::mbar_arrive_expect_tx(bar(kBarQFull), kQBytes + kWBytes);
+            ptx::tma_load_2d_hint(sbase + kOffQ, &tm_q, bar(kBarQFull), 0, b0 * kRows * kHeads,
+                                  ptx::policy_evict_first());
+            ptx::tma_load_2d(sbase + kOffW, &tm_w, bar(kBarQFull), 0, b0 * kRows);
+        } else {
+            ptx::mbar_arrive(bar(kBarQFull));
+        }
+        ptx::prefetch_tensormap(&tm_k);
     }
     if (warp == kMmaWarp0) {
         ptx::tmem_alloc(sbase + kOffMisc, kTmemCols);
@@ -540,13 +549,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t pol_q = ptx::policy_evict_first();
         uint32_t ui = 0, g = 0, qi = 0;
         // Claim the next unit with key tiles (empty units are skipped here, never published);
-        // every lane returns the same unit, lane r < kRows also its row's window.
+        // every lane returns the same unit, lane r < kRows also its row's window.  Units below
+        // gridDim.x are the CTAs' static first units; the shared counter hands out the rest.
+        // When every unit is a first unit, the counter is never touched.
+        const bool dynamic = uint32_t(p.num_units) > gridDim.x;
         auto claim = [&]() -> Geometry {
             while (true) {
                 uint32_t u = 0;
                 int stop = 0;
                 if (lane == 0) {
-                    u = atomicAdd(&p.sched->next_unit, 1u);
+                    u = dynamic ? gridDim.x + atomicAdd(&p.sched->next_unit, 1u) : uint32_t(p.num_units);
                     stop = (u >= uint32_t(p.num_units) || *abort_flag) ? 1 : 0;
                 }
                 u = __shfl_sync(0xffffffffu, u, 0);
@@ -561,14 +573,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // Move the shared counter past the chunks of this block that this claim has
                 // shown to be empty, so no CTA spends a claim on them (a hint: a unit that is
                 // claimed anyway is found empty).
-                if (lane == 0 && geo.skip > 0)
-                    atomicMax(&p.sched->next_unit, u - uint32_t(c) + uint32_t(geo.skip));
+                const uint32_t next_useful = u - uint32_t(c) + uint32_t(geo.skip);
+                if (lane == 0 && geo.skip > 0 && next_useful > gridDim.x)
+                    atomicMax(&p.sched->next_unit, next_useful - gridDim.x);
                 if (geo.t1 > geo.t0) return geo;
             }
         };
         // Publish a unit to the consumers (m0 < 0: the terminate marker) and start its Q + w
         // load.  Returns false when the CTA is aborting.
-        auto publish = [&](const Geometry& geo) -> bool {
+        auto publish = [&](const Geometry& geo, bool q_requested) -> bool {
             const uint32_t slot = ui % kUnitSlots;
             int ok = 1;
             if (lane == 0) ok = wait_bar(bar(kBarUnitEmpty + slot), ((ui / kUnitSlots) & 1u) ^ 1u, ctl);
@@ -588,7 +601,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) {
                 ptx::mbar_arrive(bar(kBarUnitFull + slot));
-                if (geo.m0 >= 0) {
+                if (geo.m0 >= 0 && q_requested) {
+                    ++qi;
+                } else if (geo.m0 >= 0) {
                     const uint32_t qs = qi % kQSlots;
                     ok = wait_bar(bar(kBarQEmpty + qs), ((qi / kQSlots) & 1u) ^ 1u, ctl);
                     if (ok) {
@@ -614,8 +629,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         // while the current unit's last kClaimAhead K tiles are still to be issued (plus the
         // kStages in the ring), so the claim's global round trips and the Q load hide behind
         // them.  Claiming earlier would hold units back from CTAs that finish first.
-        Geometry cur = claim();
-        bool ok = publish(cur);
+        // The static first unit is published even when it has no key tiles (its Q is already
+        // on the way); the consumers then skip it.
+        Geometry cur = unit_geometry(p, p.num_blocks - 1 - int32_t(blockIdx.x / uint32_t(p.split)),
+                                     int32_t(blockIdx.x % uint32_t(p.split)), true);
+        if (lane == 0 && cur.skip > 0) {
+            const uint32_t next_useful = blockIdx.x - blockIdx.x % uint32_t(p.split) + uint32_t(cur.skip);
+            if (dynamic && next_useful > gridDim.x)
+                atomicMax(&p.sched->next_unit, next_useful - gridDim.x);
+        }
+        bool ok = publish(cur, true);
         while (ok && cur.m0 >= 0) {
             Geometry nxt{};
             bool have_nxt = false;
@@ -623,7 +646,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int32_t t = cur.t0; ok && t < cur.t1; ++t) {
                 if (t == claim_at) {
                     nxt = claim();
-                    ok = publish(nxt);
+                    ok = publish(nxt, false);
                     have_nxt = true;
                     if (!ok) break;
                 }
@@ -647,7 +670,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (ok && !have_nxt) {
                 nxt = claim();
-                ok = publish(nxt);
+                ok = publish(nxt, false);
             }
             cur = nxt;
         }
@@ -728,11 +751,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::fence_proxy_async_smem();  // visible to the bulk copies
                 __syncwarp();
             }
-            while (true) {
+            // the CTA's own index first, then the shared counter (untouched when every unit is
+            // a first unit)
+            const bool dynamic = uint32_t(p.num_units) > gridDim.x;
+            for (bool first = true;; first = false) {
                 uint32_t u = 0;
                 int stop = 0;
                 if (lane == 0) {
-                    u = atomicAdd(&p.sched->next_fill, 1u);
+                    u = first ? blockIdx.x
+                              : (dynamic ? gridDim.x + atomicAdd(&p.sched->next_fill, 1u)
+                                         : uint32_t(p.num_units));
                     stop = (u >= uint32_t(p.num_units) || *abort_flag) ? 1 : 0;
                 }
                 u = __shfl_sync(0xffffffffu, u, 0);
@@ -894,7 +922,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem_base, kTmemCols);
     }
-    if (threadIdx.x == 0) {
+    if (threadIdx.x == 0 && uint32_t(p.num_units) > gridDim.x) {
+        // the shared counters were used: the last CTA out resets them for the slot's next launch
         __threadfence();
         const uint32_t prev = atomicAdd(&p.sched->done_ctas, 1u);
         if (prev == gridDim.x - 1) {
