@@ -51,6 +51,8 @@ REFERENCE_BUDGET_S = 90.0  # CPU seconds for a whole --impl reference run
 # The per-workload block: (workload, clean_logits, split_n); split_n 0 is the default.
 WORKLOAD_TABLE = [
     ("tiny_causal_64x256", 1, 0),
+    ("small_causal_128x4096", 1, 0),
+    ("small_causal_1024x1024", 1, 0),
     ("causal_8192x8192", 0, 0),
     ("chunk_causal_4096x32768", 1, 0),
     ("chunk_causal_4096x32768", 0, 0),
@@ -286,6 +288,24 @@ def time_calls(fm, args_dev, out, clean, split_n, steps, warmup, flush, stream, 
     return [s.elapsed_time(e) for s, e in zip(starts, ends)], clocks.summary()
 
 
+def back_to_back_us(fm, args_dev, out, clean, split_n, calls, stream, dev):
+    """Mean µs per call over `calls` calls issued back to back between two events."""
+    import torch
+    for _ in range(10):
+        fm.fp8_mqa_logits(*args_dev, out=out, clean_logits=bool(clean), split_n=split_n,
+                          stream=stream)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(calls):
+        fm.fp8_mqa_logits(*args_dev, out=out, clean_logits=bool(clean), split_n=split_n,
+                          stream=stream)
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    if fm.check_error(stream) != 0:
+        raise RuntimeError("device status after back-to-back calls is not OK")
+    return 1e3 * a.elapsed_time(b) / calls
+
+
 def workload_block(fm, dev, stream, flush, steps, warmup, fp8_peak, hbm_peak, sm_count):
     """Every configuration of WORKLOAD_TABLE timed like the headline call."""
     import torch
@@ -302,6 +322,11 @@ def workload_block(fm, dev, stream, flush, steps, warmup, fp8_peak, hbm_peak, sm
         out = torch.empty((inp["M"], inp["N"]), dtype=torch.float32, device=dev)
         ms, clocks = time_calls(fm, args_dev, out, clean, split_n, steps, warmup, flush,
                                 stream, dev)
+        back_to_back = None
+        if inp["M"] * inp["N"] <= (1 << 22):
+            # small problems: also the mean over calls issued back to back (no flush between
+            # them), where a call's launch overlaps the previous call's execution
+            back_to_back = back_to_back_us(fm, args_dev, out, clean, split_n, 200, stream, dev)
         del out
         mean_s = statistics.mean(ms) * 1e-3
         flops = valid_flops(inp)
@@ -313,7 +338,7 @@ def workload_block(fm, dev, stream, flush, steps, warmup, fp8_peak, hbm_peak, sm
             "us_per_call": mean_s * 1e6, "us_min": min(ms) * 1e3,
             "tflops": flops / mean_s / 1e12, "frac_of_fp8_peak": flops / mean_s / 1e12 / fp8_peak,
             "hbm_gbs": nbytes / mean_s / 1e9, "frac_of_hbm": nbytes / mean_s / 1e9 / hbm_peak,
-            "clocks": clocks})
+            "us_per_call_back_to_back": back_to_back, "clocks": clocks})
     return rows
 
 
@@ -533,6 +558,53 @@ def run_split_sweep(args):
     return 0
 
 
+def run_family_sweep(args):
+    """Time every window family at the workload's shape (the page's op-test families), with
+    the computed key tiles and valid pairs of each, so that the cost of rows that share a
+    block with longer rows (time follows the block's window union) shows."""
+    import torch
+
+    import fp8_mqa_logits_02_gb300 as fm
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    fm.lib()
+    wl = workloads.WORKLOADS[args.workload]
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    q, k, kv, w = workloads.draw(wl.M, wl.N, wl.seed)
+    out = torch.empty((wl.M, wl.N), dtype=torch.float32, device=dev)
+    rows = []
+    for fam in workloads.WINDOW_FAMILIES:
+        ks, ke = workloads.windows(fam, wl.M, wl.N, wl.requests if wl.requests > 1 else 4)
+        inp = {"q": q, "k": k, "kv_scale": kv, "w": w, "ks": ks, "ke": ke, "M": wl.M,
+               "N": wl.N, "H": wl.H, "D": wl.D}
+        args_dev = _device_inputs(inp, dev)
+        ms, clocks = time_calls(fm, args_dev, out, args.clean, args.split_n, args.steps,
+                                args.warmup, flush, stream, dev)
+        pairs = workloads.valid_pairs(ks, ke, wl.N)
+        # key tiles the kernel computes: per 8-row block, the tiles meeting its window union
+        lo = np.clip(ks.astype(np.int64), 0, wl.N)
+        hi = np.clip(ke.astype(np.int64), 0, wl.N)
+        tiles = 0
+        for b in range(0, wl.M, 8):
+            l, h = lo[b:b + 8], hi[b:b + 8]
+            live = h > l
+            if live.any():
+                tiles += int(-(-h[live].max() // 128) - l[live].min() // 128)
+        us = statistics.mean(ms) * 1e3
+        rows.append({"family": fam, "us_per_call": us, "valid_pairs": pairs,
+                     "computed_pairs": tiles * 128 * 8,
+                     "valid_fraction_of_computed": pairs / max(1, tiles * 128 * 8),
+                     "ns_per_valid_kpair": us * 1e6 / max(1, pairs),
+                     "ns_per_computed_kpair": us * 1e6 / max(1, tiles * 128 * 8),
+                     "sm_mhz": clocks["sm_mhz"] if clocks else None})
+    print(json.dumps({"metric": "window families at one shape, µs per call",
+                      "shape": f"{wl.M}x{wl.N}", "clean_logits": args.clean,
+                      "steps": args.steps, "table": rows}), flush=True)
+    return 0
+
+
 # Revision tag of the kernel the committed ncu traffic figure was taken on.
 KERNEL_REV = "v6"
 
@@ -551,6 +623,8 @@ def parse_args(argv=None):
                     help="skip the per-workload block (the headline call only)")
     ap.add_argument("--topk", type=int, default=0,
                     help="time the per-row top-k (this k) over the workload's logits instead")
+    ap.add_argument("--family-sweep", action="store_true",
+                    help="time every window family at the workload's shape instead")
     ap.add_argument("--sweep-split", default="",
                     help="comma-separated split_n values: time each (and the default) instead")
     ap.add_argument("--reference-rows", type=int, default=4096,
@@ -579,6 +653,8 @@ def main(argv=None):
         return run_topk(args)
     if args.sweep_split:
         return run_split_sweep(args)
+    if args.family_sweep:
+        return run_family_sweep(args)
     return run_gpu(args)
 
 

@@ -200,6 +200,8 @@ FULL_SIZE = {
     "multi_req_2048x65536": [(1, 0)],
     "multi_req_1024x131072": [(1, 0), (1, 20)],
     "multi_req_8192x8192": [(1, 0)],
+    "small_causal_1024x1024": [(1, 0), (0, 0), (1, 3)],
+    "small_causal_128x4096": [(1, 0), (0, 0)],
 }
 
 

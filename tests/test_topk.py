@@ -100,11 +100,14 @@ def test_indexer_pipeline_top512_matches_the_oracle_pipeline():
     assert same >= 0.9 * len(rows) and overlap >= 500, (same, overlap)
 
 
-@pytest.mark.parametrize("N", [3000, 20000, 40000])
+@pytest.mark.parametrize("N", [3000, 5000, 20000, 40000])
 def test_crowded_threshold_bin_takes_the_multi_pass_path(N):
-    # more entries than the threshold-bin buffer holds (1024 per warp of the row's group,
-    # at most 8192) share the top 11 key bits of the k-th largest: the select resolves the
-    # remaining bits with further passes over the row
+    # More entries than the threshold-bin buffer holds share the top 11 key bits of the k-th
+    # largest, so the select resolves the remaining bits with further passes over the row.
+    # The buffers hold 2048 entries for rows of up to 32768 keys at k <= 512 (two rows per
+    # CTA), 4096 there at k > 512, and 8192 for longer rows (one row per CTA).  So N = 3000
+    # reaches the multi-pass path at k <= 512 only, N = 5000 and 20000 at every k, and
+    # N = 40000 in the one-row kernel.
     x = np.empty((5, N), dtype=np.float32)
     x[0] = 1.0                                            # all equal: ties in index order
     x[1] = 1.0 + np.arange(N, dtype=np.float32) * 2.0 ** -23   # distinct, one top bin

@@ -62,6 +62,9 @@ WORKLOADS = {
                                       requests=4),
     "multi_req_8192x8192": Workload("multi_req_8192x8192", 8192, 8192, "multi_req", 10,
                                     requests=4),
+    # The small shape the page's "Known limitations" names (M <= 128 and 1024 x 1024).
+    "small_causal_1024x1024": Workload("small_causal_1024x1024", 1024, 1024, "causal", 11),
+    "small_causal_128x4096": Workload("small_causal_128x4096", 128, 4096, "causal", 12),
 }
 
 WINDOW_FAMILIES = ("causal", "cp", "misaligned", "empty", "past_end", "multi_req")
