@@ -95,7 +95,9 @@ void init_device(int dev, DeviceState& st)
                              int(2 * sizeof(TopkSmemPair))) != cudaSuccess ||
         cudaFuncSetAttribute(topk_kernel<TopkSmemPairWide>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             int(2 * sizeof(TopkSmemPairWide))) != cudaSuccess) {
+                             int(2 * sizeof(TopkSmemPairWide))) != cudaSuccess ||
+        cudaFuncSetAttribute(topk_reg_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(kTopkRegRows * sizeof(TopkRegSmem))) != cudaSuccess) {
         st.init_status = FP8MQA_ERR_LAUNCH;
         return;
     }
@@ -652,7 +654,15 @@ int fp8_mqa_topk(const float* logits, int64_t M, int64_t N, int64_t ld, int32_t 
     // the select's re-reads.  Rows of up to 32768 keys go two per CTA.
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int64_t pair_grid = (M + 1) / 2 < st->sm_count ? (M + 1) / 2 : st->sm_count;
-    if (N <= 32768 && k <= 512) {
+    if (N <= fp8mqa::kTopkRegKeys && k <= fp8mqa::kTopkRegMaxK) {
+        // rows of up to 8192 keys stay in registers, four rows per CTA
+        const int64_t rows_per_cta = fp8mqa::kTopkRegRows;
+        const int64_t reg_grid = (M + rows_per_cta - 1) / rows_per_cta < st->sm_count
+                                     ? (M + rows_per_cta - 1) / rows_per_cta
+                                     : st->sm_count;
+        fp8mqa::topk_reg_kernel<<<dim3(uint32_t(reg_grid)), fp8mqa::kTopkThreads,
+                                  fp8mqa::kTopkRegRows * sizeof(fp8mqa::TopkRegSmem), s>>>(p);
+    } else if (N <= 32768 && k <= 512) {
         fp8mqa::topk_kernel<fp8mqa::TopkSmemPair><<<dim3(uint32_t(pair_grid)),
                                                       fp8mqa::kTopkThreads,
                                                       2 * sizeof(fp8mqa::TopkSmemPair), s>>>(p);

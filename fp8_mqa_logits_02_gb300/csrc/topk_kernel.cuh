@@ -667,4 +667,166 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkParams 
     }
 }
 
+// ---------------------------------------------------------------------------------------
+// Rows of up to kTopkRegKeys keys and k <= kTopkRegMaxK: the row stays in registers.
+//
+// Four rows per 512-thread CTA, 128 threads per row on a named barrier of its own; thread t
+// holds keys [64 t, 64 t + 64) of its row (one read of the row, 16-byte loads).  Three radix
+// passes over those registers (key bits 31..21, 20..10, 9..0; shared-memory histograms, only
+// the keys that still match the prefix taking part after the first) fix the k-th largest key
+// T and how many of the keys equal to T are taken, the lowest indices first.  One compaction
+// by block scans, in index order, then writes the winners, and the winners are sorted.
+constexpr int kTopkRegThreads = 128;                  // threads per row
+constexpr int kTopkRegRows = kTopkThreads / kTopkRegThreads;
+constexpr int kTopkRegPerThread = 64;                 // keys per thread
+constexpr int kTopkRegKeys = kTopkRegThreads * kTopkRegPerThread;  // 8192
+constexpr int kTopkRegMaxK = 1024;
+
+struct TopkRegSmem {
+    static constexpr int kNT = kTopkRegThreads;
+    uint32_t hist[kTopkBins];
+    unsigned long long win[kTopkRegMaxK];
+    unsigned long long tmp[kTopkRegMaxK];
+    uint32_t scratch[kTopkRegThreads / 32];
+    uint32_t sel_bin, sel_above, sel_count, pad;
+};
+static_assert(kTopkRegRows * sizeof(TopkRegSmem) <= 232448, "top-k shared memory");
+static_assert(sizeof(TopkRegSmem) % 16 == 0, "row slices stay 16-byte aligned");
+
+// One radix pass over the registers: histogram of (key >> shift) & (nb - 1) for the keys whose
+// bits above `shift + log2(nb)` equal `prefix` under `pmask`, then the bin of the kk-th
+// largest among them (s.sel_bin, s.sel_above).  Returns the number of keys counted.  Uniform
+// over the row's threads.
+template <int E>
+__device__ __forceinline__ uint32_t topk_reg_pass(TopkRegSmem& s, const uint32_t (&key)[E],
+                                              uint32_t prefix, uint32_t pmask, int shift,
+                                              uint32_t nb, uint32_t kk)
+{
+    constexpr int NT = kTopkRegThreads;
+    const int tid = topk_tid<NT>();
+    for (uint32_t b = tid; b < nb; b += NT) s.hist[b] = 0;
+    topk_sync<NT>();
+#pragma unroll
+    for (int j = 0; j < E; ++j) {
+        const uint32_t kj = key[j];
+        if (kj != 0u && (kj & pmask) == prefix) atomicAdd(&s.hist[(kj >> shift) & (nb - 1)], 1u);
+    }
+    topk_sync<NT>();
+    return topk_find_bin(s, s.hist, nb, kk);
+}
+
+__global__ void __launch_bounds__(kTopkThreads, 1) topk_reg_kernel(const TopkParams p)
+{
+    constexpr int NT = kTopkRegThreads;
+    constexpr int E = kTopkRegPerThread;
+    extern __shared__ __align__(16) uint8_t topk_smem_raw[];
+    const int slot = int(threadIdx.x) / NT;
+    TopkRegSmem& s = reinterpret_cast<TopkRegSmem*>(topk_smem_raw)[slot];
+    const int tid = topk_tid<NT>();
+    const int N = int(p.N);
+    const uint32_t k = uint32_t(p.k);
+    const int base = E * tid;  // this thread's first key
+
+    for (int64_t row = int64_t(blockIdx.x) * kTopkRegRows + slot; row < p.M;
+         row += int64_t(gridDim.x) * kTopkRegRows) {
+        const float* x = p.logits + row * p.ld;
+
+        // ---- 1. the thread's keys (0: not eligible or past N)
+        uint32_t key[E];
+        if ((reinterpret_cast<uintptr_t>(x) & 15u) == 0 && base + E <= N) {
+#pragma unroll
+            for (int q = 0; q < E / 4; ++q) {
+                const float4 v = __ldg(reinterpret_cast<const float4*>(x + base + 4 * q));
+                key[4 * q + 0] = topk_eligible(v.x) ? topk_key(v.x) : 0u;
+                key[4 * q + 1] = topk_eligible(v.y) ? topk_key(v.y) : 0u;
+                key[4 * q + 2] = topk_eligible(v.z) ? topk_key(v.z) : 0u;
+                key[4 * q + 3] = topk_eligible(v.w) ? topk_key(v.w) : 0u;
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < E; ++j) {
+                const int i = base + j;
+                const float v = i < N ? __ldg(x + i) : __int_as_float(0xff800000u);
+                key[j] = topk_eligible(v) ? topk_key(v) : 0u;
+            }
+        }
+
+        // ---- 2. the k-th largest key T, and kk: how many keys equal to T are taken
+        // (ineligible keys are 0 and never counted: the first pass's total is the number of
+        // eligible keys)
+        const uint32_t total = topk_reg_pass(s, key, 0u, 0u, 21, 2048u, k);
+        uint32_t T, kk;
+        if (total <= k) {
+            T = 0u;  // every eligible key (> 0) is a winner
+            kk = 0u;
+        } else {
+            const uint32_t b0 = s.sel_bin, above0 = s.sel_above;
+            topk_sync<NT>();
+            topk_reg_pass(s, key, b0 << 21, 0x7FFu << 21, 10, 2048u, k - above0);
+            const uint32_t b1 = s.sel_bin, above1 = s.sel_above;
+            topk_sync<NT>();
+            const uint32_t prefix = (b0 << 21) | (b1 << 10);
+            topk_reg_pass(s, key, prefix, 0xFFFFFC00u, 0, 1024u, k - above0 - above1);
+            const uint32_t b2 = s.sel_bin, above2 = s.sel_above;
+            T = prefix | b2;
+            kk = k - above0 - above1 - above2;  // >= 1: T itself is among the winners
+            topk_sync<NT>();
+        }
+
+        // ---- 3. the winners, in index order: keys above T, and the first kk keys equal to T
+        uint32_t n_eq = 0;
+#pragma unroll
+        for (int j = 0; j < E; ++j) n_eq += (T != 0u && key[j] == T) ? 1u : 0u;
+        uint32_t eq_total = 0;
+        const uint32_t eq_before = topk_block_scan<NT>(n_eq, s.scratch, eq_total) - n_eq;
+        uint32_t n_take = 0;
+        {
+            uint32_t r = eq_before;
+#pragma unroll
+            for (int j = 0; j < E; ++j) {
+                const bool eq = T != 0u && key[j] == T;
+                n_take += (key[j] > T || (eq && r < kk)) ? 1u : 0u;
+                r += eq ? 1u : 0u;
+            }
+        }
+        uint32_t n_sel = 0;
+        uint32_t pos = topk_block_scan<NT>(n_take, s.scratch, n_sel) - n_take;
+        {
+            uint32_t r = eq_before;
+#pragma unroll
+            for (int j = 0; j < E; ++j) {
+                const bool eq = T != 0u && key[j] == T;
+                if (key[j] > T || (eq && r < kk))
+                    s.win[pos++] = topk_composite(key[j], base + j);
+                r += eq ? 1u : 0u;
+            }
+        }
+        topk_sync<NT>();
+
+        // ---- 4. order the winners and write the row
+        topk_sort_winners<NT>(s.win, s.tmp, int(n_sel));
+        int32_t* oi = p.indices + row * int64_t(k);
+        float* ov = p.values ? p.values + row * int64_t(k) : nullptr;
+        for (int j = tid; j < int(k); j += NT) {
+            int32_t idx = -1;
+            float val = __int_as_float(0xff800000);
+            if (j < int(n_sel)) {
+                const unsigned long long cv = s.win[j];
+                idx = int32_t(0xFFFFFFFFu - uint32_t(cv & 0xFFFFFFFFull));
+                const uint32_t kj = uint32_t(cv >> 32);
+                if (kj == 0x80000000u) {
+                    // a zero: the key folded its sign away, so read it back (the guard keeps
+                    // the read in bounds)
+                    val = uint32_t(idx) < uint32_t(N) ? x[idx] : __int_as_float(0x7fc00000);
+                } else {
+                    val = __uint_as_float((kj & 0x80000000u) ? (kj & 0x7FFFFFFFu) : ~kj);
+                }
+            }
+            oi[j] = idx;
+            if (ov) ov[j] = val;
+        }
+        topk_sync<NT>();
+    }
+}
+
 }  // namespace fp8mqa

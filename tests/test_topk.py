@@ -117,3 +117,27 @@ def test_crowded_threshold_bin_takes_the_multi_pass_path(N):
     x[4] = 1.0 + (np.arange(N) % 97).astype(np.float32) * 2.0 ** -23   # many tie groups
     for k in (1, 5, 100, 1537, 2048):
         _check(x, k, what=f"crowded k={k}")
+
+
+@pytest.mark.parametrize("k", [1, 512, 1000, 1024])
+def test_full_8192_key_rows_causal_tails(k):
+    # rows of exactly 8192 keys (the register-resident path's largest), each with a window of
+    # its own length and -inf after it, as the causal logits have
+    M, N = 300, 8192
+    x = workloads.draw_logits(M, N, seed=k + 11, neg_inf_frac=0.0, empty_rows=1)
+    for m in range(M):
+        x[m, (37 * m * m + 5) % N + 1:] = -np.inf
+    _check(x, k, what=f"causal tails k={k}")
+
+
+@pytest.mark.parametrize("k", [1, 300, 512, 1024])
+def test_full_8192_key_rows_with_heavy_ties(k):
+    N = 8192
+    x = np.full((5, N), 0.25, dtype=np.float32)
+    x[1, ::2] = 0.5                                       # 4096 equal winners above the cut
+    x[2, 4000:] = np.float32(-0.0)
+    x[2, 6000:] = 0.0
+    x[3] = np.float32(1.0) + np.float32(2.0 ** -23) * (np.arange(N) % 3)   # three tie groups
+    x[4, ::5] = -np.inf
+    x[4, 3::7] = 3.0e38
+    _check(x, k, what=f"heavy ties k={k}")
