@@ -668,51 +668,148 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkParams 
 }
 
 // ---------------------------------------------------------------------------------------
-// Rows of up to kTopkRegKeys keys and k <= kTopkRegMaxK: the row stays in registers.
+// Rows of up to kTopkRegKeys keys and k <= kTopkRegMaxK: the row is staged in shared memory.
 //
-// Four rows per 512-thread CTA, 128 threads per row on a named barrier of its own; thread t
-// holds keys [64 t, 64 t + 64) of its row (one read of the row, 16-byte loads).  Three radix
-// passes over those registers (key bits 31..21, 20..10, 9..0; shared-memory histograms, only
-// the keys that still match the prefix taking part after the first) fix the k-th largest key
-// T and how many of the keys equal to T are taken, the lowest indices first.  One compaction
-// by block scans, in index order, then writes the winners, and the winners are sorted.
+// Four rows per 512-thread CTA, 128 threads per row on a named barrier of their own.  A row
+// arrives in shared memory by asynchronous copies (thread t copies elements 512 q + 4 t .. +3,
+// q < 16: each warp's copy reads 512 contiguous bytes).  Per row:
+//   1. A histogram of the top 11 key bits over every eighth element of the row gives a
+//      threshold G a little below where the k-th largest key is expected.
+//   2. One compare per key and a warp ballot mark the keys >= G (the candidates); the ballot
+//      words give each candidate's slot, and the candidates' composites go to a buffer.
+//   3. A radix select over the candidates' 64-bit composites (key, then index) finds the cut:
+//      exactly min(k, eligible) composites are >= it.  The composites are unique, so the cut
+//      resolves ties at the k-th value by index without a separate tie step.
+//   4. The winners are sorted and written.
+// When the threshold misses (fewer than k eligible candidates, or more than the buffer holds),
+// step 3 runs over the whole staged row instead.  The next row's copies are issued as soon as
+// the staged row is no longer read, so they land during the selection and the sort.
 constexpr int kTopkRegThreads = 128;                  // threads per row
 constexpr int kTopkRegRows = kTopkThreads / kTopkRegThreads;
 constexpr int kTopkRegPerThread = 64;                 // keys per thread
 constexpr int kTopkRegKeys = kTopkRegThreads * kTopkRegPerThread;  // 8192
 constexpr int kTopkRegMaxK = 1024;
+constexpr int kTopkRegCap = 2048;                     // candidate buffer (composites)
 
 struct TopkRegSmem {
     static constexpr int kNT = kTopkRegThreads;
-    uint32_t hist[kTopkBins];
-    unsigned long long win[kTopkRegMaxK];
-    unsigned long long tmp[kTopkRegMaxK];
+    float row[kTopkRegKeys];
+    // the candidates; the winners' sort uses its first kTopkRegMaxK entries as scratch once
+    // the candidates are spent
+    unsigned long long cand[kTopkRegCap];
+    // the winners; before them the same bytes hold the sample histogram, then the ballots,
+    // then the cut's histograms
+    union {
+        unsigned long long win[kTopkRegMaxK];
+        uint32_t hist[kTopkBins];
+        uint32_t ballots[kTopkRegThreads / 32][kTopkRegPerThread];
+    };
     uint32_t scratch[kTopkRegThreads / 32];
-    uint32_t sel_bin, sel_above, sel_count, pad;
+    uint32_t sel_bin, sel_above, sel_count, n_win, n_bad, pad[3];
 };
 static_assert(kTopkRegRows * sizeof(TopkRegSmem) <= 232448, "top-k shared memory");
 static_assert(sizeof(TopkRegSmem) % 16 == 0, "row slices stay 16-byte aligned");
+static_assert(kTopkRegMaxK <= kTopkRegCap, "the sort's scratch fits in the candidate buffer");
 
-// One radix pass over the registers: histogram of (key >> shift) & (nb - 1) for the keys whose
-// bits above `shift + log2(nb)` equal `prefix` under `pmask`, then the bin of the kk-th
-// largest among them (s.sel_bin, s.sel_above).  Returns the number of keys counted.  Uniform
-// over the row's threads.
-template <int E>
-__device__ __forceinline__ uint32_t topk_reg_pass(TopkRegSmem& s, const uint32_t (&key)[E],
-                                              uint32_t prefix, uint32_t pmask, int shift,
-                                              uint32_t nb, uint32_t kk)
+// The row element in key slot j of thread tid.
+__device__ __forceinline__ int topk_reg_elem(int tid, int j)
+{
+    return 512 * (j >> 2) + 4 * tid + (j & 3);
+}
+
+// Start the asynchronous copy of a row's elements in this thread's slots to `dst` (-inf past
+// N).  16-byte copies when the row is 16-byte aligned, else 4-byte ones.
+__device__ __forceinline__ void topk_reg_stage(float* dst, const float* x, int N, int tid)
+{
+    const bool aligned = (reinterpret_cast<uintptr_t>(x) & 15u) == 0;
+#pragma unroll 4
+    for (int q = 0; q < kTopkRegPerThread / 4; ++q) {
+        const int e = topk_reg_elem(tid, 4 * q);
+        const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst + e));
+        if (aligned && e + 3 < N) {
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(x + e)
+                         : "memory");
+        } else {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                if (e + c < N)
+                    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(d + 4u * c),
+                                 "l"(x + e + c)
+                                 : "memory");
+                else
+                    dst[e + c] = __int_as_float(0xff800000u);
+            }
+        }
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// Wait for this thread's staged copies (a hardware wait: no spin).
+__device__ __forceinline__ void topk_reg_stage_wait()
+{
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+}
+
+// Composite of an element (0 when it is not eligible: 0 sorts below every eligible entry).
+__device__ __forceinline__ unsigned long long topk_reg_comp(float v, int i)
+{
+    return topk_eligible(v) ? topk_composite(topk_key(v), i) : 0ull;
+}
+
+// topk_append with a capacity: an entry past `cap` is dropped (the selection hands over at
+// most `cap` winners, so none is; the guard keeps a wrong count inside the buffer).
+__device__ __forceinline__ void topk_append_capped(unsigned long long* buf, uint32_t* count,
+                                                   unsigned long long v, bool take, uint32_t cap)
+{
+    const uint32_t mask = __ballot_sync(0xffffffffu, take);
+    if (mask == 0) return;
+    const int lane = threadIdx.x & 31;
+    const int leader = __ffs(mask) - 1;
+    uint32_t base = 0;
+    if (lane == leader) base = atomicAdd(count, uint32_t(__popc(mask)));
+    base = __shfl_sync(0xffffffffu, base, leader);
+    const uint32_t at = base + uint32_t(__popc(mask & ((1u << lane) - 1u)));
+    if (take && at < cap) buf[at] = v;
+}
+
+// The cut: the largest value such that exactly min(k, n) of the row's nonzero composites are
+// >= it (n: how many there are); 1 when n <= k.  Radix passes of 8 bits over the composite's
+// key (bits 63..32), then over the index part (bits 15..0).  Bits 31..16 are all ones for
+// every index below 2^16, so they join the prefix before the index passes.  A pass whose
+// selected bin is taken whole ends the search.
+// `src(fn)` calls fn(composite) for each of this thread's composites, with a trip count that
+// may differ between threads.  Uniform over the row's threads.
+template <typename Src>
+__device__ __forceinline__ unsigned long long topk_reg_cut(TopkRegSmem& s, uint32_t k, Src&& src)
 {
     constexpr int NT = kTopkRegThreads;
     const int tid = topk_tid<NT>();
-    for (uint32_t b = tid; b < nb; b += NT) s.hist[b] = 0;
-    topk_sync<NT>();
-#pragma unroll
-    for (int j = 0; j < E; ++j) {
-        const uint32_t kj = key[j];
-        if (kj != 0u && (kj & pmask) == prefix) atomicAdd(&s.hist[(kj >> shift) & (nb - 1)], 1u);
+    unsigned long long prefix = 0ull, mask = 0ull;
+    uint32_t need = k;
+#pragma unroll 1
+    for (int pass = 0; pass < 6; ++pass) {
+        const int sh = pass < 4 ? 56 - 8 * pass : 8 * (5 - pass);
+        if (pass == 4) {
+            prefix |= 0xFFFF0000ull;
+            mask |= 0xFFFF0000ull;
+        }
+        s.hist[tid] = 0u;
+        s.hist[tid + NT] = 0u;
+        topk_sync<NT>();
+        src([&](unsigned long long c) {
+            if (c != 0ull && (c & mask) == prefix) atomicAdd(&s.hist[uint32_t(c >> sh) & 255u], 1u);
+        });
+        topk_sync<NT>();
+        const uint32_t total = topk_find_bin(s, s.hist, 256u, need);
+        if (pass == 0 && total <= need) return 1ull;
+        const uint32_t d = s.sel_bin, above = s.sel_above, cnt = s.sel_count;
+        topk_sync<NT>();
+        prefix |= static_cast<unsigned long long>(d) << sh;
+        mask |= 0xFFull << sh;
+        need -= above;
+        if (cnt == need) break;  // the whole bin is taken: every composite >= prefix wins
     }
-    topk_sync<NT>();
-    return topk_find_bin(s, s.hist, nb, kk);
+    return prefix;
 }
 
 __global__ void __launch_bounds__(kTopkThreads, 1) topk_reg_kernel(const TopkParams p)
@@ -723,94 +820,128 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_reg_kernel(const TopkPar
     const int slot = int(threadIdx.x) / NT;
     TopkRegSmem& s = reinterpret_cast<TopkRegSmem*>(topk_smem_raw)[slot];
     const int tid = topk_tid<NT>();
+    const int lane = tid & 31, warp = tid >> 5;
     const int N = int(p.N);
     const uint32_t k = uint32_t(p.k);
-    const int base = E * tid;  // this thread's first key
+    const int64_t row_step = int64_t(gridDim.x) * kTopkRegRows;
+    // sampled keys needed above the threshold: an eighth of k plus a margin of about two
+    // standard deviations of the sampled count
+    const uint32_t r = (k >> 3) + (k >> 5) + 6u;
 
-    for (int64_t row = int64_t(blockIdx.x) * kTopkRegRows + slot; row < p.M;
-         row += int64_t(gridDim.x) * kTopkRegRows) {
+    int64_t row = int64_t(blockIdx.x) * kTopkRegRows + slot;
+    if (row < p.M) topk_reg_stage(s.row, p.logits + row * p.ld, N, tid);
+    for (; row < p.M; row += row_step) {
         const float* x = p.logits + row * p.ld;
+        for (int b = tid; b < kTopkBins; b += NT) s.hist[b] = 0u;
+        if (tid == 0) {
+            s.n_win = 0u;
+            s.n_bad = 0u;
+        }
+        topk_reg_stage_wait();
+        topk_sync<NT>();  // the staged row and the cleared histogram, for every thread
 
-        // ---- 1. the thread's keys (0: not eligible or past N)
-        uint32_t key[E];
-        if ((reinterpret_cast<uintptr_t>(x) & 15u) == 0 && base + E <= N) {
+        // ---- 1. the threshold G from the sampled keys: every eighth element (those of the
+        // even threads' first slot of each chunk), so any window of the row is sampled evenly
+        if ((tid & 1) == 0) {
 #pragma unroll
             for (int q = 0; q < E / 4; ++q) {
-                const float4 v = __ldg(reinterpret_cast<const float4*>(x + base + 4 * q));
-                key[4 * q + 0] = topk_eligible(v.x) ? topk_key(v.x) : 0u;
-                key[4 * q + 1] = topk_eligible(v.y) ? topk_key(v.y) : 0u;
-                key[4 * q + 2] = topk_eligible(v.z) ? topk_key(v.z) : 0u;
-                key[4 * q + 3] = topk_eligible(v.w) ? topk_key(v.w) : 0u;
-            }
-        } else {
-#pragma unroll
-            for (int j = 0; j < E; ++j) {
-                const int i = base + j;
-                const float v = i < N ? __ldg(x + i) : __int_as_float(0xff800000u);
-                key[j] = topk_eligible(v) ? topk_key(v) : 0u;
-            }
-        }
-
-        // ---- 2. the k-th largest key T, and kk: how many keys equal to T are taken
-        // (ineligible keys are 0 and never counted: the first pass's total is the number of
-        // eligible keys)
-        const uint32_t total = topk_reg_pass(s, key, 0u, 0u, 21, 2048u, k);
-        uint32_t T, kk;
-        if (total <= k) {
-            T = 0u;  // every eligible key (> 0) is a winner
-            kk = 0u;
-        } else {
-            const uint32_t b0 = s.sel_bin, above0 = s.sel_above;
-            topk_sync<NT>();
-            topk_reg_pass(s, key, b0 << 21, 0x7FFu << 21, 10, 2048u, k - above0);
-            const uint32_t b1 = s.sel_bin, above1 = s.sel_above;
-            topk_sync<NT>();
-            const uint32_t prefix = (b0 << 21) | (b1 << 10);
-            topk_reg_pass(s, key, prefix, 0xFFFFFC00u, 0, 1024u, k - above0 - above1);
-            const uint32_t b2 = s.sel_bin, above2 = s.sel_above;
-            T = prefix | b2;
-            kk = k - above0 - above1 - above2;  // >= 1: T itself is among the winners
-            topk_sync<NT>();
-        }
-
-        // ---- 3. the winners, in index order: keys above T, and the first kk keys equal to T
-        uint32_t n_eq = 0;
-#pragma unroll
-        for (int j = 0; j < E; ++j) n_eq += (T != 0u && key[j] == T) ? 1u : 0u;
-        uint32_t eq_total = 0;
-        const uint32_t eq_before = topk_block_scan<NT>(n_eq, s.scratch, eq_total) - n_eq;
-        uint32_t n_take = 0;
-        {
-            uint32_t r = eq_before;
-#pragma unroll
-            for (int j = 0; j < E; ++j) {
-                const bool eq = T != 0u && key[j] == T;
-                n_take += (key[j] > T || (eq && r < kk)) ? 1u : 0u;
-                r += eq ? 1u : 0u;
-            }
-        }
-        uint32_t n_sel = 0;
-        uint32_t pos = topk_block_scan<NT>(n_take, s.scratch, n_sel) - n_take;
-        {
-            uint32_t r = eq_before;
-#pragma unroll
-            for (int j = 0; j < E; ++j) {
-                const bool eq = T != 0u && key[j] == T;
-                if (key[j] > T || (eq && r < kk))
-                    s.win[pos++] = topk_composite(key[j], base + j);
-                r += eq ? 1u : 0u;
+                const float f = s.row[topk_reg_elem(tid, 4 * q)];
+                if (topk_eligible(f)) atomicAdd(&s.hist[topk_key(f) >> 21], 1u);
             }
         }
         topk_sync<NT>();
+        const uint32_t sampled = topk_find_bin(s, s.hist, uint32_t(kTopkBins), r);
+        const bool lowest = sampled < r;  // few eligible keys: every one is a candidate
+        float g = -3.402823466e38f;
+        if (!lowest) {
+            // the lowest value of the selected bin (finite: bins below 4 hold only -inf and
+            // -NaN, and those keys were not counted)
+            const uint32_t kt = s.sel_bin << 21;
+            g = __uint_as_float((kt & 0x80000000u) ? (kt & 0x7FFFFFFFu) : ~kt);
+        }
+        topk_sync<NT>();  // the histogram's bytes become the ballots
+
+        // ---- 2. candidates: one ballot per key slot (+inf passes the compare and is dropped
+        // below; NaN and -inf fail it)
+#pragma unroll
+        for (int q = 0; q < E / 4; ++q) {
+            const float4 f = *reinterpret_cast<const float4*>(&s.row[topk_reg_elem(tid, 4 * q)]);
+            const uint32_t m0 = __ballot_sync(0xffffffffu, f.x >= g);
+            const uint32_t m1 = __ballot_sync(0xffffffffu, f.y >= g);
+            const uint32_t m2 = __ballot_sync(0xffffffffu, f.z >= g);
+            const uint32_t m3 = __ballot_sync(0xffffffffu, f.w >= g);
+            if (lane == 0)
+                *reinterpret_cast<uint4*>(&s.ballots[warp][4 * q]) = make_uint4(m0, m1, m2, m3);
+        }
+        __syncwarp();
+        const uint32_t b0 = s.ballots[warp][lane], b1 = s.ballots[warp][lane + 32];
+        const uint32_t n_mine = uint32_t(__popc(b0) + __popc(b1));
+        uint32_t n_cand = 0;
+        uint32_t pos = topk_block_scan<NT>(n_mine, s.scratch, n_cand) - n_mine;
+        bool fast = n_cand <= uint32_t(kTopkRegCap) && (n_cand >= k || lowest);
+
+        unsigned long long cut = 1ull;
+        if (fast) {
+            // this lane writes the candidates of key slots `lane` and `lane + 32` of its
+            // warp: bit b of a slot's ballot is that slot's element in lane b
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int j = lane + 32 * h;
+                uint32_t bits = h ? b1 : b0;
+                while (bits) {
+                    const int b = __ffs(bits) - 1;
+                    bits &= bits - 1u;
+                    const int i = topk_reg_elem(32 * warp + b, j);
+                    const unsigned long long c = topk_reg_comp(s.row[i], i);
+                    if (c == 0ull) atomicAdd(&s.n_bad, 1u);  // +inf
+                    s.cand[pos++] = c;
+                }
+            }
+            topk_sync<NT>();
+            // a threshold above the k-th eligible key (the candidates held +inf entries)
+            if (!lowest && n_cand - s.n_bad < k) fast = false;
+        }
+        if (!fast) {
+            // the threshold missed: select over the whole staged row
+            const int n = N;
+            cut = topk_reg_cut(s, k, [&](auto&& fn) {
+                for (int i = tid; i < n; i += NT) fn(topk_reg_comp(s.row[i], i));
+            });
+            for (int i0 = 0; i0 < n; i0 += NT) {
+                const int i = i0 + tid;
+                const unsigned long long c = i < n ? topk_reg_comp(s.row[i], i) : 0ull;
+                topk_append_capped(s.win, &s.n_win, c, c != 0ull && c >= cut, k);
+            }
+        }
+        topk_sync<NT>();  // every read of the staged row is done
+
+        // ---- the next row's copies go out now
+        const int64_t next = row + row_step;
+        if (next < p.M) topk_reg_stage(s.row, p.logits + next * p.ld, N, tid);
+
+        // ---- 3. the cut over the candidates, and the winners
+        if (fast) {
+            const int nc = int(n_cand);
+            cut = topk_reg_cut(s, k, [&](auto&& fn) {
+                for (int i = tid; i < nc; i += NT) fn(s.cand[i]);
+            });
+            for (int i0 = 0; i0 < nc; i0 += NT) {
+                const int i = i0 + tid;
+                const unsigned long long c = i < nc ? s.cand[i] : 0ull;
+                topk_append_capped(s.win, &s.n_win, c, c != 0ull && c >= cut, k);
+            }
+            topk_sync<NT>();
+        }
+        const int n_sel = int(min(s.n_win, k));
 
         // ---- 4. order the winners and write the row
-        topk_sort_winners<NT>(s.win, s.tmp, int(n_sel));
+        topk_sort_winners<NT>(s.win, s.cand, n_sel);
         int32_t* oi = p.indices + row * int64_t(k);
         float* ov = p.values ? p.values + row * int64_t(k) : nullptr;
         for (int j = tid; j < int(k); j += NT) {
             int32_t idx = -1;
             float val = __int_as_float(0xff800000);
-            if (j < int(n_sel)) {
+            if (j < n_sel) {
                 const unsigned long long cv = s.win[j];
                 idx = int32_t(0xFFFFFFFFu - uint32_t(cv & 0xFFFFFFFFull));
                 const uint32_t kj = uint32_t(cv >> 32);

@@ -141,3 +141,36 @@ def test_full_8192_key_rows_with_heavy_ties(k):
     x[4, ::5] = -np.inf
     x[4, 3::7] = 3.0e38
     _check(x, k, what=f"heavy ties k={k}")
+
+
+def _sampled_positions(N):
+    # For rows of up to 8192 keys the kernel estimates its threshold from every fourth
+    # element of every other 512-element chunk (one key in eight).
+    e = np.arange(N)
+    return (e % 4 == 0) & ((e // 512) % 2 == 0)
+
+
+@pytest.mark.parametrize("k", [1, 64, 512, 1024])
+def test_threshold_estimate_misses_take_the_full_row_path(k):
+    N = 8192
+    rng = np.random.default_rng(k)
+    s = _sampled_positions(N)
+    x = rng.standard_normal((8, N)).astype(np.float32)
+    x[0, s] = 4.0 + rng.random(s.sum()).astype(np.float32)    # the estimate sees only the top
+    x[1] = 1.5
+    x[1, s] = 1.0                                              # everything unsampled is larger
+    x[2, rng.random(N) < 0.3] = np.inf                         # +inf is not eligible
+    x[3, s] = np.inf
+    x[4, ~s] = np.inf
+    x[5, rng.random(N) < 0.5] = np.nan
+    x[6, s] = -np.inf                                          # the estimate sees nothing
+    x[7, :] = -np.inf
+    x[7, ~s & (rng.random(N) < 0.2)] = 1.0                     # ties, none of them sampled
+    _check(x, k, what=f"estimate misses k={k}")
+
+
+def test_unaligned_rows_of_the_register_path():
+    wide = workloads.draw_logits(40, 8400, seed=21)
+    for off, n in ((101, 8192), (3, 8001), (2, 4097)):
+        t = torch.from_numpy(wide).cuda()[:, off:off + n]       # rows start off 16 bytes
+        _check(wide[:, off:off + n].copy(), 512, gpu_rows=t, what=f"unaligned {off}")
