@@ -204,7 +204,20 @@ __device__ __forceinline__ uint32_t topk_find_bin(S& s, const uint32_t* hist, ui
     const int tid = topk_tid<NT>();
     const int per = int(nb) / NT;
     uint32_t run = 0;
-    for (int j = 0; j < per; ++j) run += hist[nb - 1 - (tid * per + j)];
+    if (per >= 4) {
+        // the thread's bins as 16-byte reads, rotated so that the eight lanes of each
+        // quarter warp read distinct bank groups (a plain walk would put all lanes' reads on
+        // two banks); the sum does not depend on the order (hist: 16-byte aligned)
+        const int nv = per >> 2;
+        const int rot = 5 - (__ffs(per) - 1);
+        const uint32_t* base = hist + (int(nb) - per * (tid + 1));
+        for (int v = 0; v < nv; ++v) {
+            const uint4 h = *reinterpret_cast<const uint4*>(base + 4 * ((v + (tid >> rot)) & (nv - 1)));
+            run += h.x + h.y + h.z + h.w;
+        }
+    } else {
+        for (int j = 0; j < per; ++j) run += hist[nb - 1 - (tid * per + j)];
+    }
     uint32_t total = 0;
     const uint32_t incl = topk_block_scan<NT>(run, s.scratch, total);
     const uint32_t excl = incl - run;
@@ -840,14 +853,12 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_reg_kernel(const TopkPar
         topk_reg_stage_wait();
         topk_sync<NT>();  // the staged row and the cleared histogram, for every thread
 
-        // ---- 1. the threshold G from the sampled keys: every eighth element (those of the
-        // even threads' first slot of each chunk), so any window of the row is sampled evenly
-        if ((tid & 1) == 0) {
+        // ---- 1. the threshold G from the sampled keys: every eighth element, so any window
+        // of the row is sampled evenly
 #pragma unroll
-            for (int q = 0; q < E / 4; ++q) {
-                const float f = s.row[topk_reg_elem(tid, 4 * q)];
-                if (topk_eligible(f)) atomicAdd(&s.hist[topk_key(f) >> 21], 1u);
-            }
+        for (int i = 0; i < kTopkRegKeys / (8 * NT); ++i) {
+            const float f = s.row[8 * (tid + NT * i)];
+            if (topk_eligible(f)) atomicAdd(&s.hist[topk_key(f) >> 21], 1u);
         }
         topk_sync<NT>();
         const uint32_t sampled = topk_find_bin(s, s.hist, uint32_t(kTopkBins), r);
