@@ -417,15 +417,7 @@ def run_gpu(args):
     peaks = load_peaks()
     fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
     achieved = flops / per_launch_s / 1e12
-    traffic = None
-    tpath = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(tpath):
-        try:
-            tj = json.load(open(tpath))
-            if tj.get("workload") == wl.name and tj.get("kernel_rev") == KERNEL_REV:
-                traffic = tj.get("bytes_per_launch")
-        except Exception:
-            traffic = None
+    traffic = committed_traffic("fp8_mqa_logits_kernel", wl.name, KERNEL_REV)
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws,
@@ -504,6 +496,7 @@ def run_topk(args):
     algo_bytes = M * N * 4 + M * args.topk * 8
     peaks = load_peaks()
     gbs = algo_bytes / (ms * 1e-3) / 1e9
+    kernel = topk_kernel_name(N, args.topk)
     print(json.dumps({
         "metric": "per-row top-k over the logits, GB/s of algorithmic traffic",
         "value": gbs, "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
@@ -512,9 +505,10 @@ def run_topk(args):
         "config": {"workload": wl.name, "M": M, "N": N, "k": args.topk,
                    "l2": f"flushed before every timed call ({FLUSH_BYTES >> 20} MiB write)"},
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": gbs / peaks["hbm_gbs"], "traffic": None,
+                     "frac": gbs / peaks["hbm_gbs"],
+                     "traffic": committed_traffic(kernel, wl.name, TOPK_REV, args.topk),
                      "peak_source": f"{peaks['source']} copy bandwidth",
-                     "kernel": "topk_kernel"},
+                     "kernel": kernel, "kernel_rev": TOPK_REV},
         "gpu_launches": args.steps, "clocks": clocks.summary(),
     }), flush=True)
     return 0
@@ -605,8 +599,33 @@ def run_family_sweep(args):
     return 0
 
 
-# Revision tag of the kernel the committed ncu traffic figure was taken on.
+# Revision tags of the kernels the committed ncu traffic figures were taken on.
 KERNEL_REV = "v6"
+TOPK_REV = "t3"
+
+
+def committed_traffic(kernel, workload, rev, k=None):
+    """dram read + write bytes per launch from profiles/traffic.json for this kernel, workload,
+    revision (and k), else None: a figure taken on another revision is not reported."""
+    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        entries = json.load(open(tpath))
+    except (OSError, ValueError):
+        return None
+    for e in entries if isinstance(entries, list) else [entries]:
+        if (e.get("kernel", "fp8_mqa_logits_kernel") == kernel and e.get("workload") == workload
+                and e.get("kernel_rev") == rev and e.get("k") == k):
+            return e.get("bytes_per_launch")
+    return None
+
+
+def topk_kernel_name(N, k):
+    """The kernel fp8_mqa_topk launches for rows of N keys and this k."""
+    if N <= 8192 and k <= 1024:
+        return "topk_reg_kernel"
+    if N <= 32768:
+        return "topk_kernel<TopkSmemPair>" if k <= 512 else "topk_kernel<TopkSmemPairWide>"
+    return "topk_kernel<TopkSmemOne>"
 
 
 def parse_args(argv=None):
