@@ -119,9 +119,9 @@ def test_crowded_threshold_bin_takes_the_multi_pass_path(N):
         _check(x, k, what=f"crowded k={k}")
 
 
-@pytest.mark.parametrize("k", [1, 512, 1000, 1024])
+@pytest.mark.parametrize("k", [1, 512, 1000, 1024, 1025, 2048])
 def test_full_8192_key_rows_causal_tails(k):
-    # rows of exactly 8192 keys (the register-resident path's largest), each with a window of
+    # rows of exactly 8192 keys (the staged-row path's largest at k <= 1024), each with a window of
     # its own length and -inf after it, as the causal logits have
     M, N = 300, 8192
     x = workloads.draw_logits(M, N, seed=k + 11, neg_inf_frac=0.0, empty_rows=1)
@@ -130,7 +130,7 @@ def test_full_8192_key_rows_causal_tails(k):
     _check(x, k, what=f"causal tails k={k}")
 
 
-@pytest.mark.parametrize("k", [1, 300, 512, 1024])
+@pytest.mark.parametrize("k", [1, 300, 512, 1024, 2048])
 def test_full_8192_key_rows_with_heavy_ties(k):
     N = 8192
     x = np.full((5, N), 0.25, dtype=np.float32)
@@ -150,7 +150,7 @@ def _sampled_positions(N):
     return (e % 4 == 0) & ((e // 512) % 2 == 0)
 
 
-@pytest.mark.parametrize("k", [1, 64, 512, 1024])
+@pytest.mark.parametrize("k", [1, 64, 512, 1024, 2048])
 def test_threshold_estimate_misses_take_the_full_row_path(k):
     N = 8192
     rng = np.random.default_rng(k)
@@ -173,4 +173,5 @@ def test_unaligned_rows_of_the_register_path():
     wide = workloads.draw_logits(40, 8400, seed=21)
     for off, n in ((101, 8192), (3, 8001), (2, 4097)):
         t = torch.from_numpy(wide).cuda()[:, off:off + n]       # rows start off 16 bytes
-        _check(wide[:, off:off + n].copy(), 512, gpu_rows=t, what=f"unaligned {off}")
+        for k in (512, 2048):
+            _check(wide[:, off:off + n].copy(), k, gpu_rows=t, what=f"unaligned {off} k={k}")
