@@ -600,7 +600,7 @@ def run_family_sweep(args):
 
 
 # Revision tags of the kernels the committed ncu traffic figures were taken on.
-KERNEL_REV = "v6"
+KERNEL_REV = "v7"
 TOPK_REV = "t3"
 
 

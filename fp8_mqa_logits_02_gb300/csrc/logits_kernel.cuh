@@ -532,6 +532,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ptx::prefetch_tensormap(&tm_k);
     }
+    if (warp == kFillWarp) {
+        // The first unit's window words and its chunk's first two K tiles head for L2 now, so
+        // the producer's window reads and first K loads after the set-up barrier find them
+        // there (prefetches only: nothing waits on them).
+        const int32_t b0 = p.num_blocks - 1 - int32_t(blockIdx.x / uint32_t(p.split));
+        const int32_t c0 = int32_t(blockIdx.x % uint32_t(p.split));
+        if (lane < 2 && b0 >= 0 && int64_t(b0) * kRows < p.M)
+            ptx::prefetch_l2((lane ? p.ke : p.ks) + int64_t(b0) * kRows);
+        const int32_t ct0 = c0 * p.tiles_per_chunk;
+        const int32_t ct1 = min(ct0 + p.tiles_per_chunk, p.num_tiles);
+        const int32_t t = ct0 + lane - 2;
+        if (lane >= 2 && lane < 4 && t < ct1) ptx::tma_prefetch_2d(&tm_k, 0, t * kTileKeys);
+    }
     if (warp == kMmaWarp0) {
         ptx::tmem_alloc(sbase + kOffMisc, kTmemCols);
         ptx::tmem_relinquish();

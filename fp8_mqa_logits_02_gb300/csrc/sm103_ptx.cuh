@@ -116,6 +116,21 @@ __device__ __forceinline__ uint64_t policy_evict_first()
     return p;
 }
 
+// Pull one global line into L2 (no register result).
+__device__ __forceinline__ void prefetch_l2(const void* ptr)
+{
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
+}
+
+// Pull one box of a 2-D tensor map into L2 (a TMA prefetch: no shared memory, no barrier).
+__device__ __forceinline__ void tma_prefetch_2d(const void* tmap, int32_t x, int32_t y)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(tmap)),
+                 "r"(x), "r"(y)
+                 : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const void* tmap)
 {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap))
