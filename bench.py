@@ -475,13 +475,16 @@ def run_topk(args):
     inp = workloads.make(wl)
     M, N = inp["M"], inp["N"]
     t = {key: torch.from_numpy(inp[key]).to(dev) for key in ("q", "k", "kv_scale", "w", "ks", "ke")}
-    logits = fm.fp8_mqa_logits(t["q"].view(torch.float8_e4m3fn), t["k"].view(torch.float8_e4m3fn),
-                               t["kv_scale"], t["w"], t["ks"], t["ke"])
+    largs = (t["q"].view(torch.float8_e4m3fn), t["k"].view(torch.float8_e4m3fn), t["kv_scale"],
+             t["w"], t["ks"], t["ke"])
+    # --windowed: the logits without the -inf fill, and the top-k restricted to the windows
+    logits = fm.fp8_mqa_logits(*largs, clean_logits=not args.windowed)
+    win = {"ks": t["ks"], "ke": t["ke"]} if args.windowed else {}
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
     for _ in range(args.warmup):
         flush.zero_()
-        fm.topk(logits, args.topk, stream=stream)
+        fm.topk(logits, args.topk, stream=stream, **win)
     torch.cuda.synchronize(dev)
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -489,24 +492,54 @@ def run_topk(args):
         for i in range(args.steps):
             flush.zero_()
             starts[i].record(stream)
-            fm.topk(logits, args.topk, stream=stream)
+            fm.topk(logits, args.topk, stream=stream, **win)
             ends[i].record(stream)
         torch.cuda.synchronize(dev)
     ms = statistics.mean(s.elapsed_time(e) for s, e in zip(starts, ends))
-    algo_bytes = M * N * 4 + M * args.topk * 8
+    # bytes the call must move: the whole matrix, or only the windows when the top-k is windowed
+    read_elems = workloads.valid_pairs(inp["ks"], inp["ke"], N) if args.windowed else M * N
+    algo_bytes = read_elems * 4 + M * args.topk * 8
     peaks = load_peaks()
     gbs = algo_bytes / (ms * 1e-3) / 1e9
     kernel = topk_kernel_name(N, args.topk)
+
+    # the indexer step as a whole, cold: logits then top-k, in both forms
+    def pipeline(clean):
+        out = torch.empty((M, N), dtype=torch.float32, device=dev)
+        kw = {} if clean else {"ks": t["ks"], "ke": t["ke"]}
+        def step():
+            fm.fp8_mqa_logits(*largs, out=out, clean_logits=clean, stream=stream)
+            fm.topk(out, args.topk, stream=stream, **kw)
+        for _ in range(args.warmup):
+            flush.zero_()
+            step()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+        for a, b in ev:
+            flush.zero_()
+            a.record(stream)
+            step()
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        return 1e3 * statistics.mean(a.elapsed_time(b) for a, b in ev)
+
+    pipe = {"clean_logits_then_topk_us": pipeline(True),
+            "unclean_logits_then_windowed_topk_us": pipeline(False)}
     print(json.dumps({
         "metric": "per-row top-k over the logits, GB/s of algorithmic traffic",
         "value": gbs, "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms, "us_per_call": ms * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": wl.name, "M": M, "N": N, "k": args.topk,
+                   "windowed": bool(args.windowed),
+                   "read_bytes": "windows only (clean_logits=0 logits)" if args.windowed
+                   else "the whole matrix (clean_logits=1 logits)",
                    "l2": f"flushed before every timed call ({FLUSH_BYTES >> 20} MiB write)"},
+        "pipeline": pipe,
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": gbs / peaks["hbm_gbs"],
-                     "traffic": committed_traffic(kernel, wl.name, TOPK_REV, args.topk),
+                     "traffic": None if args.windowed
+                     else committed_traffic(kernel, wl.name, TOPK_REV, args.topk),
                      "peak_source": f"{peaks['source']} copy bandwidth",
                      "kernel": kernel, "kernel_rev": TOPK_REV},
         "gpu_launches": args.steps, "clocks": clocks.summary(),
@@ -642,6 +675,8 @@ def parse_args(argv=None):
                     help="skip the per-workload block (the headline call only)")
     ap.add_argument("--topk", type=int, default=0,
                     help="time the per-row top-k (this k) over the workload's logits instead")
+    ap.add_argument("--windowed", action="store_true",
+                    help="with --topk: the windowed top-k over clean_logits=0 logits")
     ap.add_argument("--family-sweep", action="store_true",
                     help="time every window family at the workload's shape instead")
     ap.add_argument("--sweep-split", default="",

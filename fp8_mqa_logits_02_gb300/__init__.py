@@ -55,6 +55,7 @@ SIGNATURES = {
     "fp8_mqa_logits_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I32,
                                               _I32, _I32, _I32, _P]),
     "fp8_mqa_topk": (ctypes.c_int, [_P, _I64, _I64, _I64, _I32, _P, _P, _P]),
+    "fp8_mqa_topk_windowed": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _P, _I32, _P, _P, _P]),
 }
 
 TOPK_MAX_K = 2048
@@ -186,25 +187,38 @@ def fp8_mqa_logits(q: torch.Tensor, k: torch.Tensor, kv_scale: torch.Tensor, w: 
     return out
 
 
-def topk(logits: torch.Tensor, k: int, with_values: bool = True, stream=None):
+def topk(logits: torch.Tensor, k: int, with_values: bool = True, stream=None,
+         ks: torch.Tensor | None = None, ke: torch.Tensor | None = None):
     """Per-row top-k of a float32 [M, N] CUDA tensor (rows may be strided, elements not).
 
     Returns (indices int32 [M, k], values float32 [M, k] or None): the k largest finite
     entries of each row, by value descending and equal values by index ascending; slots past
-    a row's finite entries hold -1 / -inf.  Asynchronous on ``stream``.
+    a row's finite entries hold -1 / -inf.  With ``ks``/``ke`` (int32 [M] on the same device,
+    the windows the logits were made with) only entries in [ks[m], ke[m]) count and nothing
+    outside them is read, so the logits may come from ``clean_logits=False``.  Asynchronous on
+    ``stream``.
     """
     _check_strided_rows(logits, "logits")
     if not 1 <= int(k) <= TOPK_MAX_K:
         raise ValueError(f"k must be in [1, {TOPK_MAX_K}]")
     M, N = logits.shape
     dev = logits.device
+    if (ks is None) != (ke is None):
+        raise ValueError("ks and ke go together")
+    for name, t in (("ks", ks), ("ke", ke)):
+        if t is not None and (t.dtype != torch.int32 or t.shape != (M,) or t.device != dev
+                              or not t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous int32 [M] tensor on {dev}")
     idx = torch.empty((M, int(k)), dtype=torch.int32, device=dev)
     val = torch.empty((M, int(k)), dtype=torch.float32, device=dev) if with_values else None
     with torch.cuda.device(dev):
-        rc = lib().fp8_mqa_topk(logits.data_ptr(), M, N, logits.stride(0), int(k), idx.data_ptr(),
-                                val.data_ptr() if val is not None else None, _stream_ptr(stream))
+        rc = lib().fp8_mqa_topk_windowed(
+            logits.data_ptr(), M, N, logits.stride(0),
+            ks.data_ptr() if ks is not None else None, ke.data_ptr() if ke is not None else None,
+            int(k), idx.data_ptr(), val.data_ptr() if val is not None else None,
+            _stream_ptr(stream))
     if rc != 0:
-        raise Fp8MqaError(rc, "fp8_mqa_topk")
+        raise Fp8MqaError(rc, "fp8_mqa_topk_windowed")
     return idx, val
 
 

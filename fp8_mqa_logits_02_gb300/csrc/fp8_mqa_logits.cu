@@ -632,12 +632,21 @@ int fp8_mqa_logits_noalloc(const uint8_t* q_fp8, const uint8_t* k_fp8, const flo
 int fp8_mqa_topk(const float* logits, int64_t M, int64_t N, int64_t ld, int32_t k,
                  int32_t* indices, float* values, void* stream)
 {
+    return fp8_mqa_topk_windowed(logits, M, N, ld, nullptr, nullptr, k, indices, values, stream);
+}
+
+int fp8_mqa_topk_windowed(const float* logits, int64_t M, int64_t N, int64_t ld,
+                          const int32_t* ks, const int32_t* ke, int32_t k, int32_t* indices,
+                          float* values, void* stream)
+{
     if (M < 0 || N < 0 || ld < N || k < 1 || k > fp8mqa::kTopkMaxK) return FP8MQA_ERR_INVALID_ARG;
     if (N > (int64_t(1) << 30)) return FP8MQA_ERR_UNSUPPORTED_SHAPE;
     if (M == 0) return FP8MQA_OK;
-    if (!indices || (N > 0 && !logits)) return FP8MQA_ERR_INVALID_ARG;
+    if (!indices || (N > 0 && !logits) || (ks == nullptr) != (ke == nullptr))
+        return FP8MQA_ERR_INVALID_ARG;
     if (!fp8mqa::aligned(logits, 4) || !fp8mqa::aligned(indices, 4) ||
-        (values && !fp8mqa::aligned(values, 4)))
+        (values && !fp8mqa::aligned(values, 4)) || (ks && !fp8mqa::aligned(ks, 4)) ||
+        (ke && !fp8mqa::aligned(ke, 4)))
         return FP8MQA_ERR_MISALIGNED;
     int err = FP8MQA_OK;
     fp8mqa::DeviceState* st = fp8mqa::device_state(&err);
@@ -650,6 +659,8 @@ int fp8_mqa_topk(const float* logits, int64_t M, int64_t N, int64_t ld, int32_t 
     p.k = k;
     p.indices = indices;
     p.values = values;
+    p.ks = ks;
+    p.ke = ke;
     // At most one CTA per SM, each walking rows: the rows in flight stay resident in L2 for
     // the select's re-reads.  Rows of up to 32768 keys go two per CTA.
     cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -38,7 +38,21 @@ struct TopkParams {
     int32_t k;
     int32_t* indices;  // [M, k]
     float* values;     // [M, k] or null
+    const int32_t* ks;  // row m's window [ks[m], ke[m]) clamped to [0, N); null: the whole row
+    const int32_t* ke;
 };
+
+// Row m's window, clamped to [0, N) (an empty window when ks >= ke).
+__device__ __forceinline__ void topk_window(const TopkParams& p, int64_t m, int& lo, int& hi)
+{
+    lo = 0;
+    hi = int(p.N);
+    if (p.ks) {
+        const int64_t a = p.ks[m], b = p.ke[m];
+        lo = int(a < 0 ? 0 : (a > p.N ? p.N : a));
+        hi = int(b < lo ? lo : (b > p.N ? p.N : b));
+    }
+}
 
 // A CTA works on kTopkThreads / NT rows at once, NT threads each, a row's threads
 // synchronising on a named barrier of their own (the whole CTA's barrier when NT is the
@@ -131,44 +145,47 @@ __device__ __forceinline__ uint32_t topk_block_scan(uint32_t v, uint32_t* scratc
     return v + before;
 }
 
-// Visit every element of the row once, in chunks whose trip count is uniform over the row's
-// threads (so warp votes inside `fn` see every lane): fn(index, value, valid).  16-byte
-// aligned rows are read four floats per thread per chunk unless kInOrder asks for one
-// element per thread per call, so that successive calls cover the row in index order.
+// Visit every element of the row's window [lo, hi) once, in chunks whose trip count is uniform
+// over the row's threads (so warp votes inside `fn` see every lane): fn(index, value, valid);
+// nothing outside the window is read.  16-byte aligned rows are read four floats per thread
+// per chunk (from lo rounded down to a multiple of 4) unless kInOrder asks for one element per
+// thread per call, so that successive calls cover the window in index order.
 template <int NT, bool kInOrder = false, typename Fn>
-__device__ __forceinline__ void topk_for_row(const float* x, int N, Fn&& fn)
+__device__ __forceinline__ void topk_for_row(const float* x, int lo, int hi, Fn&& fn)
 {
     const int tid = topk_tid<NT>();
+    auto in = [&](int i) { return i >= lo && i < hi; };
     if (!kInOrder && (reinterpret_cast<uintptr_t>(x) & 15u) == 0) {
         // four 16-byte loads in flight per thread before any is used
         constexpr int kU = 4;
-        for (int c0 = 0; c0 < N; c0 += 4 * kU * NT) {
+        for (int c0 = lo & ~3; c0 < hi; c0 += 4 * kU * NT) {
             float4 v[kU];
 #pragma unroll
             for (int u = 0; u < kU; ++u) {
                 const int i = c0 + 4 * (u * NT + tid);
                 v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (i + 3 < N) {
+                if (i >= lo && i + 3 < hi) {
                     v[u] = __ldg(reinterpret_cast<const float4*>(x + i));
                 } else {
-                    if (i < N) v[u].x = __ldg(x + i);
-                    if (i + 1 < N) v[u].y = __ldg(x + i + 1);
-                    if (i + 2 < N) v[u].z = __ldg(x + i + 2);
+                    if (in(i)) v[u].x = __ldg(x + i);
+                    if (in(i + 1)) v[u].y = __ldg(x + i + 1);
+                    if (in(i + 2)) v[u].z = __ldg(x + i + 2);
+                    if (in(i + 3)) v[u].w = __ldg(x + i + 3);
                 }
             }
 #pragma unroll
             for (int u = 0; u < kU; ++u) {
                 const int i = c0 + 4 * (u * NT + tid);
-                fn(i, v[u].x, i < N);
-                fn(i + 1, v[u].y, i + 1 < N);
-                fn(i + 2, v[u].z, i + 2 < N);
-                fn(i + 3, v[u].w, i + 3 < N);
+                fn(i, v[u].x, in(i));
+                fn(i + 1, v[u].y, in(i + 1));
+                fn(i + 2, v[u].z, in(i + 2));
+                fn(i + 3, v[u].w, in(i + 3));
             }
         }
     } else {
-        for (int c0 = 0; c0 < N; c0 += NT) {
+        for (int c0 = lo; c0 < hi; c0 += NT) {
             const int i = c0 + tid;
-            fn(i, i < N ? __ldg(x + i) : 0.f, i < N);
+            fn(i, i < hi ? __ldg(x + i) : 0.f, i < hi);
         }
     }
 }
@@ -536,6 +553,8 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkParams 
     for (int64_t row = int64_t(blockIdx.x) * kRowsPerCta + slot; row < p.M;
          row += int64_t(gridDim.x) * kRowsPerCta) {
         const float* x = p.logits + row * p.ld;
+        int lo, hi;
+        topk_window(p, row, lo, hi);
 
         // ---- 1. top 11 key bits, one histogram per warp, then their sum
         if constexpr (S::kHW == NT / 32) {
@@ -546,7 +565,7 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkParams 
             for (int b = tid; b < S::kHW * kTopkBins; b += NT) (&s.whist[0][0])[b] = 0;
             topk_sync<NT>();
         }
-        topk_for_row<NT>(x, N, [&](int, float v, bool valid) {
+        topk_for_row<NT>(x, lo, hi, [&](int, float v, bool valid) {
             const bool in = valid && topk_eligible(v);
             topk_hist_add(my_hist, in ? (topk_key(v) >> 21) : 0u, in);
         });
@@ -576,7 +595,7 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkParams 
             unsigned long long* const spare = reinterpret_cast<unsigned long long*>(&s.whist[0][0]);
             unsigned long long* const dst = take_all ? s.cand : s.tbuf;
             uint32_t* const cnt = take_all ? &s.n_cand : &s.n_tie;
-            topk_for_row<NT>(x, N, [&](int i, float v, bool valid) {
+            topk_for_row<NT>(x, lo, hi, [&](int i, float v, bool valid) {
                 const bool in = valid && topk_eligible(v);
                 const uint32_t key = in ? topk_key(v) : 0u;
                 topk_append(dst, cnt, topk_composite(key, i), in && (take_all || (key >> 21) >= b0));
@@ -611,7 +630,7 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkParams 
                 const uint32_t nb = pass == 1 ? 2048u : 1024u;
                 for (uint32_t b = tid; b < nb; b += NT) s.hist[b] = 0;
                 topk_sync<NT>();
-                topk_for_row<NT>(x, N, [&](int, float v, bool valid) {
+                topk_for_row<NT>(x, lo, hi, [&](int, float v, bool valid) {
                     bool in = valid && topk_eligible(v);
                     const uint32_t key = in ? topk_key(v) : 0u;
                     in = in && (key & pmask) == prefix;
@@ -646,9 +665,9 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkParams 
                 topk_append(s.cand, &s.n_cand, topk_composite(key, i), take);
             };
             if (ordered_ties)
-                topk_for_row<NT, true>(x, N, collect);
+                topk_for_row<NT, true>(x, lo, hi, collect);
             else
-                topk_for_row<NT>(x, N, collect);
+                topk_for_row<NT>(x, lo, hi, collect);
             topk_sync<NT>();
         }
 
@@ -730,22 +749,30 @@ __device__ __forceinline__ int topk_reg_elem(int tid, int j)
     return 512 * (j >> 2) + 4 * tid + (j & 3);
 }
 
-// Start the asynchronous copy of a row's elements in this thread's slots to `dst` (-inf past
-// N).  16-byte copies when the row is 16-byte aligned, else 4-byte ones.
-__device__ __forceinline__ void topk_reg_stage(float* dst, const float* x, int N, int tid)
+// The 512-element chunks of a row that meet its window [lo, hi): [q_lo, q_hi).
+__device__ __forceinline__ int topk_reg_qlo(int lo) { return lo >> 9; }
+__device__ __forceinline__ int topk_reg_qhi(int lo, int hi) { return hi > lo ? (hi + 511) >> 9 : lo >> 9; }
+
+// Start the asynchronous copy of a row's window [lo, hi) to `dst`: the chunks that meet the
+// window, with -inf in their slots outside it (chunks outside the window are left as they
+// are and never read).  16-byte copies where a slot group lies inside the window and the row
+// is 16-byte aligned, else 4-byte ones.
+__device__ __forceinline__ void topk_reg_stage(float* dst, const float* x, int lo, int hi, int tid)
 {
     const bool aligned = (reinterpret_cast<uintptr_t>(x) & 15u) == 0;
+    const int q_lo = topk_reg_qlo(lo), q_hi = topk_reg_qhi(lo, hi);
 #pragma unroll 4
     for (int q = 0; q < kTopkRegPerThread / 4; ++q) {
+        if (q < q_lo || q >= q_hi) continue;
         const int e = topk_reg_elem(tid, 4 * q);
         const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst + e));
-        if (aligned && e + 3 < N) {
+        if (aligned && e >= lo && e + 3 < hi) {
             asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(x + e)
                          : "memory");
         } else {
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
-                if (e + c < N)
+                if (e + c >= lo && e + c < hi)
                     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(d + 4u * c),
                                  "l"(x + e + c)
                                  : "memory");
@@ -842,9 +869,14 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_reg_kernel(const TopkPar
     const uint32_t r = (k >> 3) + (k >> 5) + 6u;
 
     int64_t row = int64_t(blockIdx.x) * kTopkRegRows + slot;
-    if (row < p.M) topk_reg_stage(s.row, p.logits + row * p.ld, N, tid);
+    int lo = 0, hi = 0;  // the row's window
+    if (row < p.M) {
+        topk_window(p, row, lo, hi);
+        topk_reg_stage(s.row, p.logits + row * p.ld, lo, hi, tid);
+    }
     for (; row < p.M; row += row_step) {
         const float* x = p.logits + row * p.ld;
+        const int q_lo = topk_reg_qlo(lo), q_hi = topk_reg_qhi(lo, hi);
         for (int b = tid; b < kTopkBins; b += NT) s.hist[b] = 0u;
         if (tid == 0) {
             s.n_win = 0u;
@@ -857,7 +889,8 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_reg_kernel(const TopkPar
         // of the row is sampled evenly
 #pragma unroll
         for (int i = 0; i < kTopkRegKeys / (8 * NT); ++i) {
-            const float f = s.row[8 * (tid + NT * i)];
+            const int e = 8 * (tid + NT * i);
+            const float f = e >= lo && e < hi ? s.row[e] : __int_as_float(0xff800000u);
             if (topk_eligible(f)) atomicAdd(&s.hist[topk_key(f) >> 21], 1u);
         }
         topk_sync<NT>();
@@ -876,6 +909,11 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_reg_kernel(const TopkPar
         // below; NaN and -inf fail it)
 #pragma unroll
         for (int q = 0; q < E / 4; ++q) {
+            if (q < q_lo || q >= q_hi) {  // outside the window: no candidates
+                if (lane == 0)
+                    *reinterpret_cast<uint4*>(&s.ballots[warp][4 * q]) = make_uint4(0u, 0u, 0u, 0u);
+                continue;
+            }
             const float4 f = *reinterpret_cast<const float4*>(&s.row[topk_reg_elem(tid, 4 * q)]);
             const uint32_t m0 = __ballot_sync(0xffffffffu, f.x >= g);
             const uint32_t m1 = __ballot_sync(0xffffffffu, f.y >= g);
@@ -913,14 +951,13 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_reg_kernel(const TopkPar
             if (!lowest && n_cand - s.n_bad < k) fast = false;
         }
         if (!fast) {
-            // the threshold missed: select over the whole staged row
-            const int n = N;
+            // the threshold missed: select over the whole staged window
             cut = topk_reg_cut(s, k, [&](auto&& fn) {
-                for (int i = tid; i < n; i += NT) fn(topk_reg_comp(s.row[i], i));
+                for (int i = lo + tid; i < hi; i += NT) fn(topk_reg_comp(s.row[i], i));
             });
-            for (int i0 = 0; i0 < n; i0 += NT) {
+            for (int i0 = lo; i0 < hi; i0 += NT) {
                 const int i = i0 + tid;
-                const unsigned long long c = i < n ? topk_reg_comp(s.row[i], i) : 0ull;
+                const unsigned long long c = i < hi ? topk_reg_comp(s.row[i], i) : 0ull;
                 topk_append_capped(s.win, &s.n_win, c, c != 0ull && c >= cut, k);
             }
         }
@@ -928,7 +965,11 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_reg_kernel(const TopkPar
 
         // ---- the next row's copies go out now
         const int64_t next = row + row_step;
-        if (next < p.M) topk_reg_stage(s.row, p.logits + next * p.ld, N, tid);
+        int next_lo = 0, next_hi = 0;
+        if (next < p.M) {
+            topk_window(p, next, next_lo, next_hi);
+            topk_reg_stage(s.row, p.logits + next * p.ld, next_lo, next_hi, tid);
+        }
 
         // ---- 3. the cut over the candidates, and the winners
         if (fast) {
@@ -968,6 +1009,8 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_reg_kernel(const TopkPar
             if (ov) ov[j] = val;
         }
         topk_sync<NT>();
+        lo = next_lo;
+        hi = next_hi;
     }
 }
 

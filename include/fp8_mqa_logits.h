@@ -227,6 +227,24 @@ FP8MQA_API int fp8_mqa_logits_noalloc(const uint8_t* q_fp8, const uint8_t* k_fp8
 FP8MQA_API int fp8_mqa_topk(const float* logits, int64_t M, int64_t N, int64_t ld, int32_t k,
                             int32_t* indices, float* values, void* stream);
 
+/*
+ * fp8_mqa_topk_windowed -- fp8_mqa_topk restricted to each row's key window: row m's result
+ * is the top-k of logits[m, n] for n in [ks[m], ke[m]) (clamped to [0, N); empty when
+ * ks[m] >= ke[m]), with the same order, tie rule and padding.  Entries outside the window are
+ * never read, so the logits may come from fp8_mqa_logits with clean_logits = 0 (whatever lies
+ * outside the windows is ignored), and only the windows' bytes are read.  With the windows that
+ * made the logits, the result equals fp8_mqa_topk's on the clean_logits = 1 output.  The page
+ * has no such entry; it is this library's way to let the consumer skip the -inf fill.
+ *
+ *   ks, ke   DEVICE int32 [M], 4-byte aligned, the same windows as fp8_mqa_logits takes; both
+ *            null gives fp8_mqa_topk.  Not modified.
+ *   the other arguments and the errors are fp8_mqa_topk's; ks without ke (or the reverse) is
+ *   FP8MQA_ERR_INVALID_ARG.
+ */
+FP8MQA_API int fp8_mqa_topk_windowed(const float* logits, int64_t M, int64_t N, int64_t ld,
+                                     const int32_t* ks, const int32_t* ke, int32_t k,
+                                     int32_t* indices, float* values, void* stream);
+
 /* fp8_mqa_logits_strerror -- a static, human-readable name for a status code. */
 FP8MQA_API const char* fp8_mqa_logits_strerror(int status);
 

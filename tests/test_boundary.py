@@ -161,3 +161,15 @@ def test_topk_rejects_bad_arguments_before_device_work(lib):
         -2
     assert f(p + 2, 4, 10, 10, 5, p, p, None) == -3
     assert f(p, 4, 10, 10, 5, p, p + 1, None) == -3
+
+
+def test_windowed_topk_rejects_bad_arguments_before_device_work(lib):
+    p = 0x1000
+    f = lib.fp8_mqa_topk_windowed
+    assert f(p, 0, 10, 10, p, p, 5, p, p, None) == 0               # no rows: nothing to do
+    assert f(p, 4, 10, 10, p, None, 5, p, p, None) == -1           # ks without ke
+    assert f(p, 4, 10, 10, None, p, 5, p, p, None) == -1           # ke without ks
+    assert f(p, 4, 10, 10, p, p, 0, p, p, None) == -1
+    assert f(p, 4, 10, 9, p, p, 5, p, p, None) == -1               # ld < N
+    assert f(p, 4, 10, 10, p + 2, p, 5, p, p, None) == -3          # ks misaligned
+    assert f(p, 4, 10, 10, p, p + 1, 5, p, p, None) == -3          # ke misaligned

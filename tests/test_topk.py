@@ -175,3 +175,62 @@ def test_unaligned_rows_of_the_register_path():
         t = torch.from_numpy(wide).cuda()[:, off:off + n]       # rows start off 16 bytes
         for k in (512, 2048):
             _check(wide[:, off:off + n].copy(), k, gpu_rows=t, what=f"unaligned {off} k={k}")
+
+
+def _windows(M, N, rng):
+    # random windows, with empty ones, windows off either end and whole rows
+    a = rng.integers(-50, N + 50, size=M)
+    b = a + rng.integers(-20, N, size=M)
+    a[::7], b[::7] = 0, N
+    a[3::11], b[3::11] = N // 2, N // 2
+    return a.astype(np.int32), b.astype(np.int32)
+
+
+def _check_windowed(x, ks, ke, k, what):
+    # the oracle sees the matrix with everything outside the windows made -inf
+    M, N = x.shape
+    ref = np.full_like(x, -np.inf)
+    for m in range(M):
+        lo, hi = max(int(ks[m]), 0), min(int(ke[m]), N)
+        if lo < hi:
+            ref[m, lo:hi] = x[m, lo:hi]
+    poisoned = x.copy()
+    for m in range(M):                    # garbage outside the windows: never read
+        lo, hi = max(int(ks[m]), 0), min(int(ke[m]), N)
+        poisoned[m, :max(lo, 0)] = np.nan
+        poisoned[m, max(hi, 0):] = 3.0e38
+    t = torch.from_numpy(poisoned).cuda()
+    idx, val = fm.topk(t, k, ks=torch.from_numpy(ks).cuda(), ke=torch.from_numpy(ke).cuda())
+    torch.cuda.synchronize()
+    ri, rv = topk_rows(ref, k)
+    gi, gv = idx.cpu().numpy(), val.cpu().numpy()
+    bad = np.nonzero((gi != ri).any(axis=1))[0]
+    assert len(bad) == 0, f"{what}: {len(bad)} rows differ, first {bad[0]}: " \
+                          f"gpu {gi[bad[0]][:8]} oracle {ri[bad[0]][:8]}"
+    assert np.array_equal(gv.view(np.uint32), rv.view(np.uint32)), what
+
+
+@pytest.mark.parametrize("M,N", [(300, 8192), (200, 5000), (64, 1000), (40, 20000), (8, 40000)])
+@pytest.mark.parametrize("k", [1, 64, 512, 1024, 2048])
+def test_windowed_rows_ignore_everything_outside_the_window(M, N, k):
+    rng = np.random.default_rng(M + N + k)
+    x = workloads.draw_logits(M, N, seed=N + k, neg_inf_frac=0.1)
+    ks, ke = _windows(M, N, rng)
+    _check_windowed(x, ks, ke, k, f"windowed {M}x{N} k={k}")
+
+
+def test_windowed_topk_on_unclean_logits_equals_topk_on_clean_logits():
+    from gpu_helpers import to_device
+    for name in ("multi_req_8192x8192", "causal_8192x8192"):
+        wl = workloads.WORKLOADS[name]
+        dev = to_device(workloads.make(wl))
+        args = (dev["q"], dev["k"], dev["kv_scale"], dev["w"], dev["ks"], dev["ke"])
+        clean = fm.fp8_mqa_logits(*args)
+        raw = torch.full_like(clean, float("nan"))
+        fm.fp8_mqa_logits(*args, out=raw, clean_logits=False)   # outside the windows: NaN
+        for k in (512, 2048):
+            i0, v0 = fm.topk(clean, k)
+            i1, v1 = fm.topk(raw, k, ks=dev["ks"], ke=dev["ke"])
+            torch.cuda.synchronize()
+            assert torch.equal(i0, i1) and torch.equal(v0.view(torch.int32), v1.view(torch.int32)), \
+                f"{name} k={k}"
