@@ -60,6 +60,48 @@ void load_encode()
     }
 }
 
+
+// Every top-k kernel's dynamic shared memory limit, for the whole-row (kWin = false) and the
+// windowed instantiations.
+template <bool kWin>
+bool topk_set_smem()
+{
+    const auto attr = cudaFuncAttributeMaxDynamicSharedMemorySize;
+    return cudaFuncSetAttribute(topk_kernel<TopkSmemOne, kWin>, attr, int(sizeof(TopkSmemOne))) ==
+               cudaSuccess &&
+           cudaFuncSetAttribute(topk_kernel<TopkSmemPair, kWin>, attr,
+                                int(2 * sizeof(TopkSmemPair))) == cudaSuccess &&
+           cudaFuncSetAttribute(topk_kernel<TopkSmemPairWide, kWin>, attr,
+                                int(2 * sizeof(TopkSmemPairWide))) == cudaSuccess &&
+           cudaFuncSetAttribute(topk_reg_kernel<kWin>, attr,
+                                int(kTopkRegRows * sizeof(TopkRegSmem))) == cudaSuccess;
+}
+
+// One launch of the top-k for rows of N keys: the staged-row kernel for rows of up to 8192 keys
+// at k <= 1024, two rows per CTA up to 32768 keys, one row per CTA beyond; at most one CTA per SM,
+// each walking rows (the rows in flight stay resident in L2 for the select's re-reads).
+template <bool kWin>
+void topk_launch(const TopkParams& p, int64_t M, int64_t N, int32_t k, int sm_count, cudaStream_t s)
+{
+    const int64_t pair_grid = (M + 1) / 2 < sm_count ? (M + 1) / 2 : sm_count;
+    if (N <= kTopkRegKeys && k <= kTopkRegMaxK) {
+        const int64_t rows = (M + kTopkRegRows - 1) / kTopkRegRows;
+        const int64_t grid = rows < sm_count ? rows : sm_count;
+        topk_reg_kernel<kWin><<<dim3(uint32_t(grid)), kTopkThreads,
+                                kTopkRegRows * sizeof(TopkRegSmem), s>>>(p);
+    } else if (N <= 32768 && k <= 512) {
+        topk_kernel<TopkSmemPair, kWin><<<dim3(uint32_t(pair_grid)), kTopkThreads,
+                                          2 * sizeof(TopkSmemPair), s>>>(p);
+    } else if (N <= 32768) {
+        topk_kernel<TopkSmemPairWide, kWin><<<dim3(uint32_t(pair_grid)), kTopkThreads,
+                                              2 * sizeof(TopkSmemPairWide), s>>>(p);
+    } else {
+        const int64_t grid = M < sm_count ? M : sm_count;
+        topk_kernel<TopkSmemOne, kWin><<<dim3(uint32_t(grid)), kTopkThreads,
+                                         sizeof(TopkSmemOne), s>>>(p);
+    }
+}
+
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 // One-time per-device setup: architecture check, kernel attributes, library buffers.
@@ -89,15 +131,7 @@ void init_device(int dev, DeviceState& st)
     }
     if (cudaFuncSetAttribute(fp8_mqa_logits_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              int(kSmemBytes)) != cudaSuccess ||
-        cudaFuncSetAttribute(topk_kernel<TopkSmemOne>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             int(sizeof(TopkSmemOne))) != cudaSuccess ||
-        cudaFuncSetAttribute(topk_kernel<TopkSmemPair>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             int(2 * sizeof(TopkSmemPair))) != cudaSuccess ||
-        cudaFuncSetAttribute(topk_kernel<TopkSmemPairWide>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             int(2 * sizeof(TopkSmemPairWide))) != cudaSuccess ||
-        cudaFuncSetAttribute(topk_reg_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             int(kTopkRegRows * sizeof(TopkRegSmem))) != cudaSuccess) {
+        !topk_set_smem<false>() || !topk_set_smem<true>()) {
         st.init_status = FP8MQA_ERR_LAUNCH;
         return;
     }
@@ -661,31 +695,11 @@ int fp8_mqa_topk_windowed(const float* logits, int64_t M, int64_t N, int64_t ld,
     p.values = values;
     p.ks = ks;
     p.ke = ke;
-    // At most one CTA per SM, each walking rows: the rows in flight stay resident in L2 for
-    // the select's re-reads.  Rows of up to 32768 keys go two per CTA.
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const int64_t pair_grid = (M + 1) / 2 < st->sm_count ? (M + 1) / 2 : st->sm_count;
-    if (N <= fp8mqa::kTopkRegKeys && k <= fp8mqa::kTopkRegMaxK) {
-        // rows of up to 8192 keys stay in registers, four rows per CTA
-        const int64_t rows_per_cta = fp8mqa::kTopkRegRows;
-        const int64_t reg_grid = (M + rows_per_cta - 1) / rows_per_cta < st->sm_count
-                                     ? (M + rows_per_cta - 1) / rows_per_cta
-                                     : st->sm_count;
-        fp8mqa::topk_reg_kernel<<<dim3(uint32_t(reg_grid)), fp8mqa::kTopkThreads,
-                                  fp8mqa::kTopkRegRows * sizeof(fp8mqa::TopkRegSmem), s>>>(p);
-    } else if (N <= 32768 && k <= 512) {
-        fp8mqa::topk_kernel<fp8mqa::TopkSmemPair><<<dim3(uint32_t(pair_grid)),
-                                                      fp8mqa::kTopkThreads,
-                                                      2 * sizeof(fp8mqa::TopkSmemPair), s>>>(p);
-    } else if (N <= 32768) {
-        fp8mqa::topk_kernel<fp8mqa::TopkSmemPairWide><<<dim3(uint32_t(pair_grid)),
-                                                          fp8mqa::kTopkThreads,
-                                                          2 * sizeof(fp8mqa::TopkSmemPairWide), s>>>(p);
-    } else {
-        const int64_t grid = M < st->sm_count ? M : st->sm_count;
-        fp8mqa::topk_kernel<fp8mqa::TopkSmemOne><<<dim3(uint32_t(grid)), fp8mqa::kTopkThreads,
-                                                     sizeof(fp8mqa::TopkSmemOne), s>>>(p);
-    }
+    if (ks)
+        fp8mqa::topk_launch<true>(p, M, N, k, st->sm_count, s);
+    else
+        fp8mqa::topk_launch<false>(p, M, N, k, st->sm_count, s);
     if (cudaGetLastError() != cudaSuccess) return FP8MQA_ERR_LAUNCH;
     return FP8MQA_OK;
 }

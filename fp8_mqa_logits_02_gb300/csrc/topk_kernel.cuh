@@ -149,12 +149,14 @@ __device__ __forceinline__ uint32_t topk_block_scan(uint32_t v, uint32_t* scratc
 // over the row's threads (so warp votes inside `fn` see every lane): fn(index, value, valid);
 // nothing outside the window is read.  16-byte aligned rows are read four floats per thread
 // per chunk (from lo rounded down to a multiple of 4) unless kInOrder asks for one element per
-// thread per call, so that successive calls cover the window in index order.
-template <int NT, bool kInOrder = false, typename Fn>
+// thread per call, so that successive calls cover the window in index order.  kWin = false:
+// the window is the whole row [0, hi) (lo is not looked at).
+template <int NT, bool kInOrder = false, bool kWin = true, typename Fn>
 __device__ __forceinline__ void topk_for_row(const float* x, int lo, int hi, Fn&& fn)
 {
     const int tid = topk_tid<NT>();
-    auto in = [&](int i) { return i >= lo && i < hi; };
+    if (!kWin) lo = 0;
+    auto in = [&](int i) { return (!kWin || i >= lo) && i < hi; };
     if (!kInOrder && (reinterpret_cast<uintptr_t>(x) & 15u) == 0) {
         // four 16-byte loads in flight per thread before any is used
         constexpr int kU = 4;
@@ -164,7 +166,7 @@ __device__ __forceinline__ void topk_for_row(const float* x, int lo, int hi, Fn&
             for (int u = 0; u < kU; ++u) {
                 const int i = c0 + 4 * (u * NT + tid);
                 v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (i >= lo && i + 3 < hi) {
+                if ((!kWin || i >= lo) && i + 3 < hi) {
                     v[u] = __ldg(reinterpret_cast<const float4*>(x + i));
                 } else {
                     if (in(i)) v[u].x = __ldg(x + i);
@@ -537,7 +539,7 @@ __device__ __forceinline__ void topk_sort_winners(unsigned long long* buf, unsig
     }
 }
 
-template <typename S>
+template <typename S, bool kWin>
 __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkParams p)
 {
     constexpr int NT = S::kNT;
@@ -553,8 +555,8 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkParams 
     for (int64_t row = int64_t(blockIdx.x) * kRowsPerCta + slot; row < p.M;
          row += int64_t(gridDim.x) * kRowsPerCta) {
         const float* x = p.logits + row * p.ld;
-        int lo, hi;
-        topk_window(p, row, lo, hi);
+        int lo = 0, hi = N;
+        if (kWin) topk_window(p, row, lo, hi);
 
         // ---- 1. top 11 key bits, one histogram per warp, then their sum
         if constexpr (S::kHW == NT / 32) {
@@ -565,7 +567,7 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkParams 
             for (int b = tid; b < S::kHW * kTopkBins; b += NT) (&s.whist[0][0])[b] = 0;
             topk_sync<NT>();
         }
-        topk_for_row<NT>(x, lo, hi, [&](int, float v, bool valid) {
+        topk_for_row<NT, false, kWin>(x, lo, hi, [&](int, float v, bool valid) {
             const bool in = valid && topk_eligible(v);
             topk_hist_add(my_hist, in ? (topk_key(v) >> 21) : 0u, in);
         });
@@ -595,7 +597,7 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkParams 
             unsigned long long* const spare = reinterpret_cast<unsigned long long*>(&s.whist[0][0]);
             unsigned long long* const dst = take_all ? s.cand : s.tbuf;
             uint32_t* const cnt = take_all ? &s.n_cand : &s.n_tie;
-            topk_for_row<NT>(x, lo, hi, [&](int i, float v, bool valid) {
+            topk_for_row<NT, false, kWin>(x, lo, hi, [&](int i, float v, bool valid) {
                 const bool in = valid && topk_eligible(v);
                 const uint32_t key = in ? topk_key(v) : 0u;
                 topk_append(dst, cnt, topk_composite(key, i), in && (take_all || (key >> 21) >= b0));
@@ -630,7 +632,7 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkParams 
                 const uint32_t nb = pass == 1 ? 2048u : 1024u;
                 for (uint32_t b = tid; b < nb; b += NT) s.hist[b] = 0;
                 topk_sync<NT>();
-                topk_for_row<NT>(x, lo, hi, [&](int, float v, bool valid) {
+                topk_for_row<NT, false, kWin>(x, lo, hi, [&](int, float v, bool valid) {
                     bool in = valid && topk_eligible(v);
                     const uint32_t key = in ? topk_key(v) : 0u;
                     in = in && (key & pmask) == prefix;
@@ -665,9 +667,9 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkParams 
                 topk_append(s.cand, &s.n_cand, topk_composite(key, i), take);
             };
             if (ordered_ties)
-                topk_for_row<NT, true>(x, lo, hi, collect);
+                topk_for_row<NT, true, kWin>(x, lo, hi, collect);
             else
-                topk_for_row<NT>(x, lo, hi, collect);
+                topk_for_row<NT, false, kWin>(x, lo, hi, collect);
             topk_sync<NT>();
         }
 
@@ -757,22 +759,25 @@ __device__ __forceinline__ int topk_reg_qhi(int lo, int hi) { return hi > lo ? (
 // window, with -inf in their slots outside it (chunks outside the window are left as they
 // are and never read).  16-byte copies where a slot group lies inside the window and the row
 // is 16-byte aligned, else 4-byte ones.
+// kWin = false: the window is the whole row [0, hi), and every chunk is written.
+template <bool kWin>
 __device__ __forceinline__ void topk_reg_stage(float* dst, const float* x, int lo, int hi, int tid)
 {
     const bool aligned = (reinterpret_cast<uintptr_t>(x) & 15u) == 0;
+    if (!kWin) lo = 0;
     const int q_lo = topk_reg_qlo(lo), q_hi = topk_reg_qhi(lo, hi);
 #pragma unroll 4
     for (int q = 0; q < kTopkRegPerThread / 4; ++q) {
-        if (q < q_lo || q >= q_hi) continue;
+        if (kWin && (q < q_lo || q >= q_hi)) continue;
         const int e = topk_reg_elem(tid, 4 * q);
         const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst + e));
-        if (aligned && e >= lo && e + 3 < hi) {
+        if (aligned && (!kWin || e >= lo) && e + 3 < hi) {
             asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(x + e)
                          : "memory");
         } else {
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
-                if (e + c >= lo && e + c < hi)
+                if ((!kWin || e + c >= lo) && e + c < hi)
                     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(d + 4u * c),
                                  "l"(x + e + c)
                                  : "memory");
@@ -852,6 +857,7 @@ __device__ __forceinline__ unsigned long long topk_reg_cut(TopkRegSmem& s, uint3
     return prefix;
 }
 
+template <bool kWin>
 __global__ void __launch_bounds__(kTopkThreads, 1) topk_reg_kernel(const TopkParams p)
 {
     constexpr int NT = kTopkRegThreads;
@@ -869,10 +875,10 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_reg_kernel(const TopkPar
     const uint32_t r = (k >> 3) + (k >> 5) + 6u;
 
     int64_t row = int64_t(blockIdx.x) * kTopkRegRows + slot;
-    int lo = 0, hi = 0;  // the row's window
+    int lo = 0, hi = N;  // the row's window
     if (row < p.M) {
-        topk_window(p, row, lo, hi);
-        topk_reg_stage(s.row, p.logits + row * p.ld, lo, hi, tid);
+        if (kWin) topk_window(p, row, lo, hi);
+        topk_reg_stage<kWin>(s.row, p.logits + row * p.ld, lo, hi, tid);
     }
     for (; row < p.M; row += row_step) {
         const float* x = p.logits + row * p.ld;
@@ -890,7 +896,7 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_reg_kernel(const TopkPar
 #pragma unroll
         for (int i = 0; i < kTopkRegKeys / (8 * NT); ++i) {
             const int e = 8 * (tid + NT * i);
-            const float f = e >= lo && e < hi ? s.row[e] : __int_as_float(0xff800000u);
+            const float f = !kWin || (e >= lo && e < hi) ? s.row[e] : __int_as_float(0xff800000u);
             if (topk_eligible(f)) atomicAdd(&s.hist[topk_key(f) >> 21], 1u);
         }
         topk_sync<NT>();
@@ -909,7 +915,7 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_reg_kernel(const TopkPar
         // below; NaN and -inf fail it)
 #pragma unroll
         for (int q = 0; q < E / 4; ++q) {
-            if (q < q_lo || q >= q_hi) {  // outside the window: no candidates
+            if (kWin && (q < q_lo || q >= q_hi)) {  // outside the window: no candidates
                 if (lane == 0)
                     *reinterpret_cast<uint4*>(&s.ballots[warp][4 * q]) = make_uint4(0u, 0u, 0u, 0u);
                 continue;
@@ -965,10 +971,10 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_reg_kernel(const TopkPar
 
         // ---- the next row's copies go out now
         const int64_t next = row + row_step;
-        int next_lo = 0, next_hi = 0;
+        int next_lo = 0, next_hi = N;
         if (next < p.M) {
-            topk_window(p, next, next_lo, next_hi);
-            topk_reg_stage(s.row, p.logits + next * p.ld, next_lo, next_hi, tid);
+            if (kWin) topk_window(p, next, next_lo, next_hi);
+            topk_reg_stage<kWin>(s.row, p.logits + next * p.ld, next_lo, next_hi, tid);
         }
 
         // ---- 3. the cut over the candidates, and the winners
