@@ -7,10 +7,13 @@
 // selected), ordered by value descending and, for equal values, by index ascending (-0.0
 // equals +0.0); slots past the row's finite entries get index -1 and value -inf.
 //
-// A persistent grid of at most one CTA per SM walks the rows (a row's second read comes from
-// L2): rows of up to 32768 keys two at a time, 256 threads each on a named barrier of their
-// own, so one row's barrier waits overlap the other's work; longer rows one at a time with
-// all 512 threads.  Radix select on an order-preserving 32-bit key:
+// Every kernel takes an optional window per row (fp8_mqa_topk_windowed): only entries inside
+// it are candidates, and nothing outside it is read.  Rows of up to 8192 keys at k <= 1024 go
+// to the staged-row kernel at the end of this file.  For the others, a persistent grid of at
+// most one CTA per SM walks the rows (a row's second read comes from L2): rows of up to 32768
+// keys two at a time, 256 threads each on a named barrier of their own, so one row's barrier
+// waits overlap the other's work; longer rows one at a time with all 512 threads.  Radix
+// select on an order-preserving 32-bit key:
 //   1. read the row, histogram the top 11 key bits (a private histogram per warp, so hot
 //      bins do not serialise the whole block);
 //   2. the bin b0 holding the k-th largest is found from the top;

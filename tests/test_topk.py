@@ -144,10 +144,10 @@ def test_full_8192_key_rows_with_heavy_ties(k):
 
 
 def _sampled_positions(N):
-    # For rows of up to 8192 keys the kernel estimates its threshold from every fourth
-    # element of every other 512-element chunk (one key in eight).
+    # For rows of up to 8192 keys (k <= 1024) the kernel estimates its threshold from every
+    # eighth element.
     e = np.arange(N)
-    return (e % 4 == 0) & ((e // 512) % 2 == 0)
+    return e % 8 == 0
 
 
 @pytest.mark.parametrize("k", [1, 64, 512, 1024, 2048])
@@ -169,7 +169,7 @@ def test_threshold_estimate_misses_take_the_full_row_path(k):
     _check(x, k, what=f"estimate misses k={k}")
 
 
-def test_unaligned_rows_of_the_register_path():
+def test_unaligned_rows_of_the_staged_row_path():
     wide = workloads.draw_logits(40, 8400, seed=21)
     for off, n in ((101, 8192), (3, 8001), (2, 4097)):
         t = torch.from_numpy(wide).cuda()[:, off:off + n]       # rows start off 16 bytes
