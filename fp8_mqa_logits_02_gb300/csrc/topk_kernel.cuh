@@ -12,8 +12,12 @@
 // to the staged-row kernel at the end of this file.  For the others, a persistent grid of at
 // most one CTA per SM walks the rows (a row's second read comes from L2): rows of up to 32768
 // keys two at a time, 256 threads each on a named barrier of their own, so one row's barrier
-// waits overlap the other's work; longer rows one at a time with all 512 threads.  Radix
-// select on an order-preserving 32-bit key:
+// waits overlap the other's work; longer rows one at a time with all 512 threads.  Each row
+// first tries a sampled threshold: a histogram of one 32-byte sector in eight of the window
+// gives G, one pass keeps the entries >= G in the buffer, and a radix cut over their
+// composites (key, index) picks the k winners.  When that misses (fewer than k kept, or more
+// than the buffer holds), the row takes the full radix select on an order-preserving 32-bit
+// key:
 //   1. read the row, histogram the top 11 key bits (a private histogram per warp, so hot
 //      bins do not serialise the whole block);
 //   2. the bin b0 holding the k-th largest is found from the top;
@@ -542,6 +546,68 @@ __device__ __forceinline__ void topk_sort_winners(unsigned long long* buf, unsig
     }
 }
 
+// Composite of an element (0 when it is not eligible: 0 sorts below every eligible entry).
+__device__ __forceinline__ unsigned long long topk_reg_comp(float v, int i)
+{
+    return topk_eligible(v) ? topk_composite(topk_key(v), i) : 0ull;
+}
+
+// topk_append with a capacity: an entry past `cap` is dropped (the selection hands over at
+// most `cap` winners, so none is; the guard keeps a wrong count inside the buffer).
+__device__ __forceinline__ void topk_append_capped(unsigned long long* buf, uint32_t* count,
+                                                   unsigned long long v, bool take, uint32_t cap)
+{
+    const uint32_t mask = __ballot_sync(0xffffffffu, take);
+    if (mask == 0) return;
+    const int lane = threadIdx.x & 31;
+    const int leader = __ffs(mask) - 1;
+    uint32_t base = 0;
+    if (lane == leader) base = atomicAdd(count, uint32_t(__popc(mask)));
+    base = __shfl_sync(0xffffffffu, base, leader);
+    const uint32_t at = base + uint32_t(__popc(mask & ((1u << lane) - 1u)));
+    if (take && at < cap) buf[at] = v;
+}
+
+// The cut: the largest value such that exactly min(k, n) of the row's nonzero composites are
+// >= it (n: how many there are); 1 when n <= k.  Radix passes of 8 bits over the composite's
+// key (bits 63..32), then over the index part (bits 15..0).  Bits 31..16 are all ones for
+// every index below 2^16, so they join the prefix before the index passes.  A pass whose
+// selected bin is taken whole ends the search.
+// `src(fn)` calls fn(composite) for each of this thread's composites, with a trip count that
+// may differ between threads.  Uniform over the row's threads.
+template <typename S, typename Src>
+__device__ __forceinline__ unsigned long long topk_reg_cut(S& s, uint32_t k, Src&& src)
+{
+    constexpr int NT = S::kNT;
+    constexpr uint32_t kBins = 256u < uint32_t(NT) ? uint32_t(NT) : 256u;  // scanned (>= NT)
+    const int tid = topk_tid<NT>();
+    unsigned long long prefix = 0ull, mask = 0ull;
+    uint32_t need = k;
+#pragma unroll 1
+    for (int pass = 0; pass < 6; ++pass) {
+        const int sh = pass < 4 ? 56 - 8 * pass : 8 * (5 - pass);
+        if (pass == 4) {
+            prefix |= 0xFFFF0000ull;
+            mask |= 0xFFFF0000ull;
+        }
+        for (uint32_t b = tid; b < kBins; b += NT) s.hist[b] = 0u;
+        topk_sync<NT>();
+        src([&](unsigned long long c) {
+            if (c != 0ull && (c & mask) == prefix) atomicAdd(&s.hist[uint32_t(c >> sh) & 255u], 1u);
+        });
+        topk_sync<NT>();
+        const uint32_t total = topk_find_bin(s, s.hist, kBins, need);
+        if (pass == 0 && total <= need) return 1ull;
+        const uint32_t d = s.sel_bin, above = s.sel_above, cnt = s.sel_count;
+        topk_sync<NT>();
+        prefix |= static_cast<unsigned long long>(d) << sh;
+        mask |= 0xFFull << sh;
+        need -= above;
+        if (cnt == need) break;  // the whole bin is taken: every composite >= prefix wins
+    }
+    return prefix;
+}
+
 template <typename S, bool kWin>
 __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkParams p)
 {
@@ -560,6 +626,72 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkParams 
         const float* x = p.logits + row * p.ld;
         int lo = 0, hi = N;
         if (kWin) topk_window(p, row, lo, hi);
+
+        // ---- 0. a threshold G from a sample of the window (8 of every 64 elements: one
+        // 32-byte sector in eight, so the sample reads an eighth of the row), then one pass
+        // that keeps the entries >= G in the buffer (the rest of the row is read once, here)
+        if (tid == 0) {
+            s.n_cand = 0;
+            s.n_tie = 0;
+        }
+        for (int b = tid; b < kTopkBins; b += NT) s.hist[b] = 0u;
+        topk_sync<NT>();
+        {
+            const bool aligned = (reinterpret_cast<uintptr_t>(x) & 15u) == 0;
+            for (int gi = (lo >> 6) + tid; gi < ((hi + 63) >> 6); gi += NT) {
+                const int e = gi << 6;
+                float v[8];
+                if (aligned && e >= lo && e + 7 < hi) {
+                    const float4 a = __ldg(reinterpret_cast<const float4*>(x + e));
+                    const float4 c = __ldg(reinterpret_cast<const float4*>(x + e + 4));
+                    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+                    v[4] = c.x; v[5] = c.y; v[6] = c.z; v[7] = c.w;
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        v[c] = e + c >= lo && e + c < hi ? __ldg(x + e + c) : __int_as_float(0xff800000u);
+                }
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    if (topk_eligible(v[c])) atomicAdd(&s.hist[topk_key(v[c]) >> 21], 1u);
+            }
+        }
+        topk_sync<NT>();
+        // sampled keys needed above the threshold: an eighth of k plus about two standard
+        // deviations of the sampled count
+        const uint32_t r = (uint32_t(k) >> 3) + (uint32_t(k) >> 5) + 6u;
+        const bool lowest = topk_find_bin(s, s.hist, kTopkBins, r) < r;
+        float g = -3.402823466e38f;
+        if (!lowest) {
+            const uint32_t kt = s.sel_bin << 21;  // a finite key: bins below 4 were not counted
+            g = __uint_as_float((kt & 0x80000000u) ? (kt & 0x7FFFFFFFu) : ~kt);
+        }
+        topk_for_row<NT, false, kWin>(x, lo, hi, [&](int i, float v, bool valid) {
+            const bool take = valid && v >= g && topk_eligible(v);
+            const uint32_t m = __ballot_sync(0xffffffffu, take);
+            if (m == 0) return;
+            const int lane = tid & 31, leader = __ffs(m) - 1;
+            uint32_t at = 0;
+            if (lane == leader) at = atomicAdd(&s.n_tie, uint32_t(__popc(m)));
+            at = __shfl_sync(0xffffffffu, at, leader) + uint32_t(__popc(m & ((1u << lane) - 1u)));
+            if (take && at < uint32_t(S::kTie)) s.tbuf[at] = topk_composite(topk_key(v), i);
+        });
+        topk_sync<NT>();
+        const uint32_t n_kept = s.n_tie;
+        const bool sampled = n_kept <= uint32_t(S::kTie) && (n_kept >= uint32_t(k) || lowest);
+        if (sampled) {
+            // the cut over the kept entries' composites, and the winners
+            const int nc = int(n_kept);
+            const unsigned long long cut = topk_reg_cut(s, uint32_t(k), [&](auto&& fn) {
+                for (int i = tid; i < nc; i += NT) fn(s.tbuf[i]);
+            });
+            for (int i0 = 0; i0 < nc; i0 += NT) {
+                const int i = i0 + tid;
+                const unsigned long long c = i < nc ? s.tbuf[i] : 0ull;
+                topk_append_capped(s.cand, &s.n_cand, c, c != 0ull && c >= cut, uint32_t(k));
+            }
+            topk_sync<NT>();
+        } else {
 
         // ---- 1. top 11 key bits, one histogram per warp, then their sum
         if constexpr (S::kHW == NT / 32) {
@@ -675,9 +807,10 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkParams 
                 topk_for_row<NT, false, kWin>(x, lo, hi, collect);
             topk_sync<NT>();
         }
+        }  // the sample's threshold missed
 
         // ---- 4. order the winners and write the row
-        const int n_sel = int(s.n_cand);
+        const int n_sel = int(min(s.n_cand, uint32_t(k)));
         topk_sort_winners<NT>(s.cand, reinterpret_cast<unsigned long long*>(&s.whist[0][0]), n_sel);
         int32_t* oi = p.indices + row * int64_t(k);
         float* ov = p.values ? p.values + row * int64_t(k) : nullptr;
@@ -796,68 +929,6 @@ __device__ __forceinline__ void topk_reg_stage(float* dst, const float* x, int l
 __device__ __forceinline__ void topk_reg_stage_wait()
 {
     asm volatile("cp.async.wait_group 0;" ::: "memory");
-}
-
-// Composite of an element (0 when it is not eligible: 0 sorts below every eligible entry).
-__device__ __forceinline__ unsigned long long topk_reg_comp(float v, int i)
-{
-    return topk_eligible(v) ? topk_composite(topk_key(v), i) : 0ull;
-}
-
-// topk_append with a capacity: an entry past `cap` is dropped (the selection hands over at
-// most `cap` winners, so none is; the guard keeps a wrong count inside the buffer).
-__device__ __forceinline__ void topk_append_capped(unsigned long long* buf, uint32_t* count,
-                                                   unsigned long long v, bool take, uint32_t cap)
-{
-    const uint32_t mask = __ballot_sync(0xffffffffu, take);
-    if (mask == 0) return;
-    const int lane = threadIdx.x & 31;
-    const int leader = __ffs(mask) - 1;
-    uint32_t base = 0;
-    if (lane == leader) base = atomicAdd(count, uint32_t(__popc(mask)));
-    base = __shfl_sync(0xffffffffu, base, leader);
-    const uint32_t at = base + uint32_t(__popc(mask & ((1u << lane) - 1u)));
-    if (take && at < cap) buf[at] = v;
-}
-
-// The cut: the largest value such that exactly min(k, n) of the row's nonzero composites are
-// >= it (n: how many there are); 1 when n <= k.  Radix passes of 8 bits over the composite's
-// key (bits 63..32), then over the index part (bits 15..0).  Bits 31..16 are all ones for
-// every index below 2^16, so they join the prefix before the index passes.  A pass whose
-// selected bin is taken whole ends the search.
-// `src(fn)` calls fn(composite) for each of this thread's composites, with a trip count that
-// may differ between threads.  Uniform over the row's threads.
-template <typename Src>
-__device__ __forceinline__ unsigned long long topk_reg_cut(TopkRegSmem& s, uint32_t k, Src&& src)
-{
-    constexpr int NT = kTopkRegThreads;
-    const int tid = topk_tid<NT>();
-    unsigned long long prefix = 0ull, mask = 0ull;
-    uint32_t need = k;
-#pragma unroll 1
-    for (int pass = 0; pass < 6; ++pass) {
-        const int sh = pass < 4 ? 56 - 8 * pass : 8 * (5 - pass);
-        if (pass == 4) {
-            prefix |= 0xFFFF0000ull;
-            mask |= 0xFFFF0000ull;
-        }
-        s.hist[tid] = 0u;
-        s.hist[tid + NT] = 0u;
-        topk_sync<NT>();
-        src([&](unsigned long long c) {
-            if (c != 0ull && (c & mask) == prefix) atomicAdd(&s.hist[uint32_t(c >> sh) & 255u], 1u);
-        });
-        topk_sync<NT>();
-        const uint32_t total = topk_find_bin(s, s.hist, 256u, need);
-        if (pass == 0 && total <= need) return 1ull;
-        const uint32_t d = s.sel_bin, above = s.sel_above, cnt = s.sel_count;
-        topk_sync<NT>();
-        prefix |= static_cast<unsigned long long>(d) << sh;
-        mask |= 0xFFull << sh;
-        need -= above;
-        if (cnt == need) break;  // the whole bin is taken: every composite >= prefix wins
-    }
-    return prefix;
 }
 
 template <bool kWin>
