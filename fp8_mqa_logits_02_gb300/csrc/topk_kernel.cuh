@@ -608,6 +608,78 @@ __device__ __forceinline__ unsigned long long topk_reg_cut(S& s, uint32_t k, Src
     return prefix;
 }
 
+// The sampled threshold's pass: append the composite of every finite entry >= g of the
+// window [lo, hi) to s.tbuf (the first S::kTie of them; s.n_tie counts them all).  g is
+// finite, so NaN and -inf never pass.  A 16-byte aligned row streams in chunks of kU float4
+// per thread, the next chunk's loads issued before the current chunk is examined; a float4 is
+// first tested by its largest entry, and only the warps where one passes look at its four
+// entries.  Entries outside the window load as -inf, so interior chunks carry no bounds test.
+template <typename S, bool kWin, int kU>
+__device__ __forceinline__ void topk_keep_above(S& s, const float* x, int lo, int hi, float g)
+{
+    constexpr int NT = S::kNT;
+    const int tid = topk_tid<NT>(), lane = tid & 31;
+    const float ninf = __int_as_float(0xff800000u);
+    if (!kWin) lo = 0;
+    auto keep = [&](int i, float v) {  // called by whole warps
+        const bool take = v >= g && topk_eligible(v);
+        const uint32_t m = __ballot_sync(0xffffffffu, take);
+        if (m == 0) return;
+        const int leader = __ffs(m) - 1;
+        uint32_t at = 0;
+        if (lane == leader) at = atomicAdd(&s.n_tie, uint32_t(__popc(m)));
+        at = __shfl_sync(0xffffffffu, at, leader) + uint32_t(__popc(m & ((1u << lane) - 1u)));
+        if (take && at < uint32_t(S::kTie)) s.tbuf[at] = topk_composite(topk_key(v), i);
+    };
+    if ((reinterpret_cast<uintptr_t>(x) & 15u) != 0) {
+        for (int c0 = lo; c0 < hi; c0 += NT) {
+            const int i = c0 + tid;
+            keep(i, i < hi ? __ldg(x + i) : ninf);
+        }
+        return;
+    }
+    constexpr int kChunk = 4 * kU * NT;
+    auto load = [&](float4 (&v)[kU], int c0) {
+        if ((!kWin || c0 >= lo) && c0 + kChunk <= hi) {
+#pragma unroll
+            for (int u = 0; u < kU; ++u)
+                v[u] = __ldg(reinterpret_cast<const float4*>(x + c0 + 4 * (u * NT + tid)));
+        } else {
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                const int i = c0 + 4 * (u * NT + tid);
+                if (i >= lo && i + 3 < hi) {
+                    v[u] = __ldg(reinterpret_cast<const float4*>(x + i));
+                } else {
+                    v[u].x = i >= lo && i < hi ? __ldg(x + i) : ninf;
+                    v[u].y = i + 1 >= lo && i + 1 < hi ? __ldg(x + i + 1) : ninf;
+                    v[u].z = i + 2 >= lo && i + 2 < hi ? __ldg(x + i + 2) : ninf;
+                    v[u].w = i + 3 >= lo && i + 3 < hi ? __ldg(x + i + 3) : ninf;
+                }
+            }
+        }
+    };
+    const int c_begin = lo & ~3;
+    float4 v[kU], nv[kU];
+    if (c_begin < hi) load(v, c_begin);
+    for (int c0 = c_begin; c0 < hi; c0 += kChunk) {
+        if (c0 + kChunk < hi) load(nv, c0 + kChunk);
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const float mx = fmaxf(fmaxf(v[u].x, v[u].y), fmaxf(v[u].z, v[u].w));
+            if (__any_sync(0xffffffffu, mx >= g)) {
+                const int i = c0 + 4 * (u * NT + tid);
+                keep(i, v[u].x);
+                keep(i + 1, v[u].y);
+                keep(i + 2, v[u].z);
+                keep(i + 3, v[u].w);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) v[u] = nv[u];
+    }
+}
+
 template <typename S, bool kWin>
 __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkParams p)
 {
@@ -666,16 +738,7 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkParams 
             const uint32_t kt = s.sel_bin << 21;  // a finite key: bins below 4 were not counted
             g = __uint_as_float((kt & 0x80000000u) ? (kt & 0x7FFFFFFFu) : ~kt);
         }
-        topk_for_row<NT, false, kWin>(x, lo, hi, [&](int i, float v, bool valid) {
-            const bool take = valid && v >= g && topk_eligible(v);
-            const uint32_t m = __ballot_sync(0xffffffffu, take);
-            if (m == 0) return;
-            const int lane = tid & 31, leader = __ffs(m) - 1;
-            uint32_t at = 0;
-            if (lane == leader) at = atomicAdd(&s.n_tie, uint32_t(__popc(m)));
-            at = __shfl_sync(0xffffffffu, at, leader) + uint32_t(__popc(m & ((1u << lane) - 1u)));
-            if (take && at < uint32_t(S::kTie)) s.tbuf[at] = topk_composite(topk_key(v), i);
-        });
+        topk_keep_above<S, kWin, 4>(s, x, lo, hi, g);
         topk_sync<NT>();
         const uint32_t n_kept = s.n_tie;
         const bool sampled = n_kept <= uint32_t(S::kTie) && (n_kept >= uint32_t(k) || lowest);
