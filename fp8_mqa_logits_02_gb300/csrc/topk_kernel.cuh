@@ -15,7 +15,9 @@
 // waits overlap the other's work; longer rows one at a time with all 512 threads.  Each row
 // first tries a sampled threshold: a histogram of one 32-byte sector in eight of the window
 // gives G, one pass keeps the entries >= G in the buffer, and a radix cut over their
-// composites (key, index) picks the k winners.  When that misses (fewer than k kept, or more
+// composites (key, index) picks the k winners.  That pass keeps the next chunk's loads in
+// flight while it examines the current one, and once it ends the next row's sample sectors
+// are prefetched into L2.  When that misses (fewer than k kept, or more
 // than the buffer holds), the row takes the full radix select on an order-preserving 32-bit
 // key:
 //   1. read the row, histogram the top 11 key bits (a private histogram per warp, so hot
@@ -120,6 +122,12 @@ __device__ __forceinline__ uint32_t topk_key(float x)
 __device__ __forceinline__ bool topk_eligible(float x)
 {
     return (__float_as_uint(x) & 0x7F800000u) != 0x7F800000u;  // finite
+}
+
+// Ask for the 32-byte sector at p to be brought into L2 (no register is written).
+__device__ __forceinline__ void topk_prefetch_l2(const float* p)
+{
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
 // Winners sort by this value, descending: key first, then the lower index.
@@ -740,6 +748,20 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkParams 
         }
         topk_keep_above<S, kWin, 4>(s, x, lo, hi, g);
         topk_sync<NT>();
+        {
+            // the next row's sample sectors go to L2 now, while this row's selection runs,
+            // so that row's sample pass finds them there
+            const int64_t nrow = row + int64_t(gridDim.x) * kRowsPerCta;
+            if (nrow < p.M) {
+                int nlo = 0, nhi = N;
+                if (kWin) topk_window(p, nrow, nlo, nhi);
+                const float* nx = p.logits + nrow * p.ld;
+                for (int gi = (nlo >> 6) + tid; gi < ((nhi + 63) >> 6); gi += NT) {
+                    const int e = max(gi << 6, nlo);
+                    if (e < nhi) topk_prefetch_l2(nx + e);
+                }
+            }
+        }
         const uint32_t n_kept = s.n_tie;
         const bool sampled = n_kept <= uint32_t(S::kTie) && (n_kept >= uint32_t(k) || lowest);
         if (sampled) {
