@@ -617,32 +617,35 @@ __device__ __forceinline__ unsigned long long topk_reg_cut(S& s, uint32_t k, Src
 }
 
 // The sampled threshold's pass: append the composite of every finite entry >= g of the
-// window [lo, hi) to s.tbuf (the first S::kTie of them; s.n_tie counts them all).  g is
-// finite, so NaN and -inf never pass.  A 16-byte aligned row streams in chunks of kU float4
-// per thread, the next chunk's loads issued before the current chunk is examined; a float4 is
-// first tested by its largest entry, and only the warps where one passes look at its four
-// entries.  Entries outside the window load as -inf, so interior chunks carry no bounds test.
+// window [lo, hi) to s.tbuf (the first S::kTie of them; s.n_tie counts them).  g is finite, so
+// NaN and -inf never pass.  A 16-byte aligned row streams in chunks of kU float4 per thread,
+// the next chunk's loads issued before the current chunk is examined; a float4 is first tested
+// by its largest entry, and only a lane whose float4 passes looks at its four entries, taking
+// a slot with a shared-memory atomic per kept entry (kept entries are a few per warp and
+// chunk, so this beats warp-wide ballots).  Entries outside the window load as -inf, so
+// interior chunks carry no bounds test.  Once more than S::kTie entries are kept the threshold
+// has failed (the caller then selects over the whole row), and the pass stops at the next
+// chunk; n_tie then only has to exceed S::kTie.
 template <typename S, bool kWin, int kU>
 __device__ __forceinline__ void topk_keep_above(S& s, const float* x, int lo, int hi, float g)
 {
     constexpr int NT = S::kNT;
-    const int tid = topk_tid<NT>(), lane = tid & 31;
+    const int tid = topk_tid<NT>();
     const float ninf = __int_as_float(0xff800000u);
     if (!kWin) lo = 0;
-    auto keep = [&](int i, float v) {  // called by whole warps
-        const bool take = v >= g && topk_eligible(v);
-        const uint32_t m = __ballot_sync(0xffffffffu, take);
-        if (m == 0) return;
-        const int leader = __ffs(m) - 1;
-        uint32_t at = 0;
-        if (lane == leader) at = atomicAdd(&s.n_tie, uint32_t(__popc(m)));
-        at = __shfl_sync(0xffffffffu, at, leader) + uint32_t(__popc(m & ((1u << lane) - 1u)));
-        if (take && at < uint32_t(S::kTie)) s.tbuf[at] = topk_composite(topk_key(v), i);
+    auto keep = [&](int i, float v) {
+        if (v >= g && topk_eligible(v)) {
+            const uint32_t at = atomicAdd(&s.n_tie, 1u);
+            if (at < uint32_t(S::kTie)) s.tbuf[at] = topk_composite(topk_key(v), i);
+        }
+    };
+    auto over = [&]() {
+        return *reinterpret_cast<volatile uint32_t*>(&s.n_tie) > uint32_t(S::kTie);
     };
     if ((reinterpret_cast<uintptr_t>(x) & 15u) != 0) {
-        for (int c0 = lo; c0 < hi; c0 += NT) {
+        for (int c0 = lo; c0 < hi && !over(); c0 += NT) {
             const int i = c0 + tid;
-            keep(i, i < hi ? __ldg(x + i) : ninf);
+            if (i < hi) keep(i, __ldg(x + i));
         }
         return;
     }
@@ -670,12 +673,12 @@ __device__ __forceinline__ void topk_keep_above(S& s, const float* x, int lo, in
     const int c_begin = lo & ~3;
     float4 v[kU], nv[kU];
     if (c_begin < hi) load(v, c_begin);
-    for (int c0 = c_begin; c0 < hi; c0 += kChunk) {
+    for (int c0 = c_begin; c0 < hi && !over(); c0 += kChunk) {
         if (c0 + kChunk < hi) load(nv, c0 + kChunk);
 #pragma unroll
         for (int u = 0; u < kU; ++u) {
             const float mx = fmaxf(fmaxf(v[u].x, v[u].y), fmaxf(v[u].z, v[u].w));
-            if (__any_sync(0xffffffffu, mx >= g)) {
+            if (mx >= g) {
                 const int i = c0 + 4 * (u * NT + tid);
                 keep(i, v[u].x);
                 keep(i + 1, v[u].y);
