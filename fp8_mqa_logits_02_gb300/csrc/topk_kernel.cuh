@@ -365,7 +365,8 @@ __device__ __forceinline__ void topk_sort_in_thread(unsigned long long (&v)[E], 
 #pragma unroll
         for (int j = 0; j < E; ++j) {
             if (j & S) continue;
-            const bool desc = ((tid * E + j) & size) == 0;
+            // size >= E: the direction is the thread's (the same for all its entries)
+            const bool desc = size >= E ? ((tid * E) & size) == 0 : (j & size) == 0;
             const unsigned long long a = v[j], b = v[j | S];
             if ((a < b) == desc) {
                 v[j] = b;
@@ -479,11 +480,12 @@ __device__ __forceinline__ void topk_sort_merge(unsigned long long* buf, unsigne
 #pragma unroll
             for (int stride = size >> 1; stride > 0; stride >>= 1) {
                 if (stride >= E) {
+                    // the lane's direction and side, the same for all its entries
+                    const int le = lane * E;
+                    const bool keep_max = ((le & size) == 0) == ((le & stride) == 0);
 #pragma unroll
                     for (int j = 0; j < E; ++j) {
-                        const int e = lane * E + j;
                         const unsigned long long o = __shfl_xor_sync(0xffffffffu, v[j], stride / E);
-                        const bool keep_max = ((e & size) == 0) == ((e & stride) == 0);
                         v[j] = (o > v[j]) == keep_max ? o : v[j];
                     }
                 } else if (stride == 1) {
@@ -517,10 +519,21 @@ __device__ __forceinline__ void topk_sort_merge(unsigned long long* buf, unsigne
                 hi = mid;
         }
         int i = lo, j = d - lo;
+        // the heads of both runs stay in registers; only the consumed one is reloaded
+        unsigned long long a = i < L ? A[i] : 0ull, b = j < L ? B[j] : 0ull;
 #pragma unroll
         for (int q = 0; q < E; ++q) {
-            const bool take_a = j >= L || (i < L && A[i] > B[j]);
-            dst[o0 + q] = take_a ? A[i++] : B[j++];
+            const bool take_a = j >= L || (i < L && a > b);
+            dst[o0 + q] = take_a ? a : b;
+            if (q + 1 < E) {
+                if (take_a) {
+                    ++i;
+                    a = i < L ? A[i] : 0ull;
+                } else {
+                    ++j;
+                    b = j < L ? B[j] : 0ull;
+                }
+            }
         }
         topk_sync<NT>();
         unsigned long long* t = src;
