@@ -650,7 +650,7 @@ def run_family_sweep(args):
 
 # Revision tags of the kernels the committed ncu traffic figures were taken on.
 KERNEL_REV = "v7"
-TOPK_REV = "t9"
+TOPK_REV = "t10"
 
 
 def committed_traffic(kernel, workload, rev, k=None):
@@ -672,8 +672,10 @@ def topk_kernel_name(N, k):
     """The kernel fp8_mqa_topk launches for rows of N keys and this k."""
     if N <= 8192 and k <= 1024:
         return "topk_reg_kernel"
+    if N <= 65536 and k <= 512:
+        return "topk_kernel<TopkSmemPair>"
     if N <= 32768:
-        return "topk_kernel<TopkSmemPair>" if k <= 512 else "topk_kernel<TopkSmemPairWide>"
+        return "topk_kernel<TopkSmemPairWide>"
     return "topk_kernel<TopkSmemOne>"
 
 

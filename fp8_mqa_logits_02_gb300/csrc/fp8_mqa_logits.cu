@@ -78,8 +78,11 @@ bool topk_set_smem()
 }
 
 // One launch of the top-k for rows of N keys: the staged-row kernel for rows of up to 8192 keys
-// at k <= 1024, two rows per CTA up to 32768 keys, one row per CTA beyond; at most one CTA per SM,
-// each walking rows (the rows in flight stay resident in L2 for the select's re-reads).
+// at k <= 1024; two rows per CTA up to 65536 keys at k <= 512 and up to 32768 keys at larger k;
+// one row per CTA beyond.  At most one CTA per SM, each walking rows (the rows in flight stay
+// resident in L2 for the select's re-reads).  Two rows per SM overlap one row's selection with
+// the other's reads; for longer rows one row per SM wins, as 1024 rows of 131072 keys fill
+// 304 row slots unevenly and a wider k crowds the shared per-two-warp histograms.
 template <bool kWin>
 void topk_launch(const TopkParams& p, int64_t M, int64_t N, int32_t k, int sm_count, cudaStream_t s)
 {
@@ -89,7 +92,7 @@ void topk_launch(const TopkParams& p, int64_t M, int64_t N, int32_t k, int sm_co
         const int64_t grid = rows < sm_count ? rows : sm_count;
         topk_reg_kernel<kWin><<<dim3(uint32_t(grid)), kTopkThreads,
                                 kTopkRegRows * sizeof(TopkRegSmem), s>>>(p);
-    } else if (N <= 32768 && k <= 512) {
+    } else if (N <= 65536 && k <= 512) {
         topk_kernel<TopkSmemPair, kWin><<<dim3(uint32_t(pair_grid)), kTopkThreads,
                                           2 * sizeof(TopkSmemPair), s>>>(p);
     } else if (N <= 32768) {

@@ -10,9 +10,10 @@
 // Every kernel takes an optional window per row (fp8_mqa_topk_windowed): only entries inside
 // it are candidates, and nothing outside it is read.  Rows of up to 8192 keys at k <= 1024 go
 // to the staged-row kernel at the end of this file.  For the others, a persistent grid of at
-// most one CTA per SM walks the rows (a row's second read comes from L2): rows of up to 32768
-// keys two at a time, 256 threads each on a named barrier of their own, so one row's barrier
-// waits overlap the other's work; longer rows one at a time with all 512 threads.  Each row
+// most one CTA per SM walks the rows (a row's second read comes from L2): rows of up to 65536
+// keys at k <= 512, and of up to 32768 keys at larger k, two at a time, 256 threads each on a
+// named barrier of their own, so one row's barrier waits overlap the other's work; longer rows
+// one at a time with all 512 threads.  Each row
 // first tries a sampled threshold: a histogram of one 32-byte sector in eight of the window
 // gives G, one pass keeps the entries >= G in the buffer, and a radix cut over their
 // composites (key, index) picks the k winners.  That pass keeps the next chunk's loads in
@@ -79,9 +80,10 @@ struct TopkSmem {
     uint32_t scratch[NT / 32];
     uint32_t sel_bin, sel_above, sel_count, n_cand, n_tie, tie_base, n_spare, pad;
 };
-// Rows of up to 32768 keys go two per CTA, 256 threads each: with k <= 512 a 2048-entry
-// threshold-bin buffer and a histogram per warp, with larger k a 4096-entry buffer and a
-// histogram per two warps.  Longer rows go one per CTA with the 8192-entry buffer they need.
+// Two rows per CTA, 256 threads each: rows of up to 65536 keys at k <= 512 with a 2048-entry
+// threshold-bin buffer and a histogram per warp; rows of up to 32768 keys at larger k with a
+// 4096-entry buffer and a histogram per two warps.  Longer rows go one per CTA with the
+// 8192-entry buffer.
 using TopkSmemPair = TopkSmem<256, 2048>;
 using TopkSmemPairWide = TopkSmem<256, 4096, 4>;
 using TopkSmemOne = TopkSmem<512, 8192>;
@@ -589,27 +591,39 @@ __device__ __forceinline__ void topk_append_capped(unsigned long long* buf, uint
     if (take && at < cap) buf[at] = v;
 }
 
+// Bytes of the index part that can differ between entries of a row of n keys: the index part
+// is 0xFFFFFFFF - index, so for every index below 2^(8 b) its bytes above the low b are all
+// ones.
+__device__ __forceinline__ int topk_index_bytes(int64_t n)
+{
+    return n <= (int64_t(1) << 16) ? 2 : n <= (int64_t(1) << 24) ? 3 : 4;
+}
+
 // The cut: the largest value such that exactly min(k, n) of the row's nonzero composites are
 // >= it (n: how many there are); 1 when n <= k.  Radix passes of 8 bits over the composite's
-// key (bits 63..32), then over the index part (bits 15..0).  Bits 31..16 are all ones for
-// every index below 2^16, so they join the prefix before the index passes.  A pass whose
-// selected bin is taken whole ends the search.
+// key (bits 63..32), then over the low `idx_bytes` bytes of the index part
+// (topk_index_bytes of the row length); the index part's higher bytes are all ones, so they
+// join the prefix before the index passes.  A pass whose selected bin is taken whole ends the
+// search.
 // `src(fn)` calls fn(composite) for each of this thread's composites, with a trip count that
 // may differ between threads.  Uniform over the row's threads.
 template <typename S, typename Src>
-__device__ __forceinline__ unsigned long long topk_reg_cut(S& s, uint32_t k, Src&& src)
+__device__ __forceinline__ unsigned long long topk_reg_cut(S& s, uint32_t k, int idx_bytes,
+                                                           Src&& src)
 {
     constexpr int NT = S::kNT;
     constexpr uint32_t kBins = 256u < uint32_t(NT) ? uint32_t(NT) : 256u;  // scanned (>= NT)
     const int tid = topk_tid<NT>();
     unsigned long long prefix = 0ull, mask = 0ull;
     uint32_t need = k;
+    const int passes = 4 + idx_bytes;
 #pragma unroll 1
-    for (int pass = 0; pass < 6; ++pass) {
-        const int sh = pass < 4 ? 56 - 8 * pass : 8 * (5 - pass);
-        if (pass == 4) {
-            prefix |= 0xFFFF0000ull;
-            mask |= 0xFFFF0000ull;
+    for (int pass = 0; pass < passes; ++pass) {
+        const int sh = pass < 4 ? 56 - 8 * pass : 8 * (passes - 1 - pass);
+        if (pass == 4 && idx_bytes < 4) {
+            const unsigned long long ones = (0xFFFFFFFFull << (8 * idx_bytes)) & 0xFFFFFFFFull;
+            prefix |= ones;
+            mask |= ones;
         }
         for (uint32_t b = tid; b < kBins; b += NT) s.hist[b] = 0u;
         topk_sync<NT>();
@@ -783,9 +797,10 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkParams 
         if (sampled) {
             // the cut over the kept entries' composites, and the winners
             const int nc = int(n_kept);
-            const unsigned long long cut = topk_reg_cut(s, uint32_t(k), [&](auto&& fn) {
-                for (int i = tid; i < nc; i += NT) fn(s.tbuf[i]);
-            });
+            const unsigned long long cut =
+                topk_reg_cut(s, uint32_t(k), topk_index_bytes(N), [&](auto&& fn) {
+                    for (int i = tid; i < nc; i += NT) fn(s.tbuf[i]);
+                });
             for (int i0 = 0; i0 < nc; i0 += NT) {
                 const int i = i0 + tid;
                 const unsigned long long c = i < nc ? s.tbuf[i] : 0ull;
@@ -1133,7 +1148,7 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_reg_kernel(const TopkPar
         }
         if (!fast) {
             // the threshold missed: select over the whole staged window
-            cut = topk_reg_cut(s, k, [&](auto&& fn) {
+            cut = topk_reg_cut(s, k, 2, [&](auto&& fn) {  // rows of at most 8192 keys
                 for (int i = lo + tid; i < hi; i += NT) fn(topk_reg_comp(s.row[i], i));
             });
             for (int i0 = lo; i0 < hi; i0 += NT) {
@@ -1155,7 +1170,7 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_reg_kernel(const TopkPar
         // ---- 3. the cut over the candidates, and the winners
         if (fast) {
             const int nc = int(n_cand);
-            cut = topk_reg_cut(s, k, [&](auto&& fn) {
+            cut = topk_reg_cut(s, k, 2, [&](auto&& fn) {
                 for (int i = tid; i < nc; i += NT) fn(s.cand[i]);
             });
             for (int i0 = 0; i0 < nc; i0 += NT) {

@@ -80,6 +80,28 @@ def test_long_rows():
         _check(x, k, what=f"long k={k}")
 
 
+def test_cut_resolves_ties_across_index_65536_in_long_rows():
+    # Rows of 131072 keys where the k-th largest value is a tie whose first winners lie on
+    # both sides of index 65536: the cut's index passes must cover the index's third byte.
+    # The planted values sit outside the sampled sectors (element e is sampled when
+    # e % 64 < 8), so the threshold comes from the background and the kept entries fit the
+    # buffer: the sampled path's cut is the one under test.
+    N = 131072
+    rng = np.random.default_rng(17)
+    x = (-rng.random((3, N))).astype(np.float32)          # background in (-1, 0]
+    pos = np.nonzero(np.arange(N) % 64 >= 8)[0]
+    for r in range(3):
+        top = rng.choice(pos, 300, replace=False)
+        rest = np.setdiff1d(pos, top)
+        below = rest[(rest >= 60000) & (rest < 65536)]
+        above = rest[rest >= 65536]
+        x[r, top] = 5.0
+        x[r, rng.choice(below, 100, replace=False)] = 4.0   # 1000 ties at the k-th value,
+        x[r, rng.choice(above, 900, replace=False)] = 4.0   # 100 of them below 65536
+    for k in (512, 1024, 2048):
+        _check(x, k, what=f"ties across 65536 k={k}")
+
+
 def test_indexer_pipeline_top512_matches_the_oracle_pipeline():
     # logits from the GPU kernel, then top-512 on the GPU, against top-512 of the fp64
     # oracle's logits (rounded to fp32) on sampled rows.  The logits agree only within the
@@ -100,14 +122,15 @@ def test_indexer_pipeline_top512_matches_the_oracle_pipeline():
     assert same >= 0.9 * len(rows) and overlap >= 500, (same, overlap)
 
 
-@pytest.mark.parametrize("N", [3000, 5000, 20000, 40000])
+@pytest.mark.parametrize("N", [3000, 5000, 20000, 40000, 70000])
 def test_crowded_threshold_bin_takes_the_multi_pass_path(N):
     # More entries than the threshold-bin buffer holds share the top 11 key bits of the k-th
     # largest, so the select resolves the remaining bits with further passes over the row.
-    # The buffers hold 2048 entries for rows of up to 32768 keys at k <= 512 (two rows per
-    # CTA), 4096 there at k > 512, and 8192 for longer rows (one row per CTA).  So N = 3000
-    # reaches the multi-pass path at k <= 512 only, N = 5000 and 20000 at every k, and
-    # N = 40000 in the one-row kernel.
+    # The buffers hold 2048 entries for rows of up to 65536 keys at k <= 512 (two rows per
+    # CTA), 4096 for rows of up to 32768 keys at k > 512, and 8192 for the others (one row per
+    # CTA).  So N = 3000 reaches the multi-pass path at k <= 512 only, N = 5000 and 20000 at
+    # every k, N = 40000 in the two-row kernel at k <= 512 and the one-row kernel beyond, and
+    # N = 70000 in the one-row kernel at every k.
     x = np.empty((5, N), dtype=np.float32)
     x[0] = 1.0                                            # all equal: ties in index order
     x[1] = 1.0 + np.arange(N, dtype=np.float32) * 2.0 ** -23   # distinct, one top bin
@@ -210,7 +233,8 @@ def _check_windowed(x, ks, ke, k, what):
     assert np.array_equal(gv.view(np.uint32), rv.view(np.uint32)), what
 
 
-@pytest.mark.parametrize("M,N", [(300, 8192), (200, 5000), (64, 1000), (40, 20000), (8, 40000)])
+@pytest.mark.parametrize("M,N", [(300, 8192), (200, 5000), (64, 1000), (40, 20000), (8, 40000),
+                                 (6, 70000)])
 @pytest.mark.parametrize("k", [1, 64, 512, 1024, 2048])
 def test_windowed_rows_ignore_everything_outside_the_window(M, N, k):
     rng = np.random.default_rng(M + N + k)
