@@ -650,7 +650,7 @@ def run_family_sweep(args):
 
 # Revision tags of the kernels the committed ncu traffic figures were taken on.
 KERNEL_REV = "v7"
-TOPK_REV = "t10"
+TOPK_REV = "t11"
 
 
 def committed_traffic(kernel, workload, rev, k=None):

@@ -647,9 +647,9 @@ __device__ __forceinline__ unsigned long long topk_reg_cut(S& s, uint32_t k, int
 // window [lo, hi) to s.tbuf (the first S::kTie of them; s.n_tie counts them).  g is finite, so
 // NaN and -inf never pass.  A 16-byte aligned row streams in chunks of kU float4 per thread,
 // the next chunk's loads issued before the current chunk is examined; a float4 is first tested
-// by its largest entry, and only a lane whose float4 passes looks at its four entries, taking
-// a slot with a shared-memory atomic per kept entry (kept entries are a few per warp and
-// chunk, so this beats warp-wide ballots).  Entries outside the window load as -inf, so
+// by its largest entry, and only a lane whose float4 passes looks at its four entries, claiming
+// slots for the ones it keeps with one shared-memory atomic (kept entries are a few per warp
+// and chunk, so this beats warp-wide ballots).  Entries outside the window load as -inf, so
 // interior chunks carry no bounds test.  Once more than S::kTie entries are kept the threshold
 // has failed (the caller then selects over the whole row), and the pass stops at the next
 // chunk; n_tie then only has to exceed S::kTie.
@@ -706,11 +706,26 @@ __device__ __forceinline__ void topk_keep_above(S& s, const float* x, int lo, in
         for (int u = 0; u < kU; ++u) {
             const float mx = fmaxf(fmaxf(v[u].x, v[u].y), fmaxf(v[u].z, v[u].w));
             if (mx >= g) {
+                // one slot claim for the lane's kept entries of this float4
                 const int i = c0 + 4 * (u * NT + tid);
-                keep(i, v[u].x);
-                keep(i + 1, v[u].y);
-                keep(i + 2, v[u].z);
-                keep(i + 3, v[u].w);
+                const bool t0 = v[u].x >= g && topk_eligible(v[u].x);
+                const bool t1 = v[u].y >= g && topk_eligible(v[u].y);
+                const bool t2 = v[u].z >= g && topk_eligible(v[u].z);
+                const bool t3 = v[u].w >= g && topk_eligible(v[u].w);
+                const uint32_t n = uint32_t(t0) + uint32_t(t1) + uint32_t(t2) + uint32_t(t3);
+                if (n != 0u) {
+                    uint32_t at = atomicAdd(&s.n_tie, n);
+                    auto put = [&](bool t, float f, int e) {
+                        if (t) {
+                            if (at < uint32_t(S::kTie)) s.tbuf[at] = topk_composite(topk_key(f), e);
+                            ++at;
+                        }
+                    };
+                    put(t0, v[u].x, i);
+                    put(t1, v[u].y, i + 1);
+                    put(t2, v[u].z, i + 2);
+                    put(t3, v[u].w, i + 3);
+                }
             }
         }
 #pragma unroll
