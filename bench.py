@@ -458,6 +458,10 @@ def run_gpu(args):
         "gpu_launches": args.steps,
         "clocks": clocks,
     }
+    if ws == 1 and not args.no_workloads and args.clean:
+        # the headline's logits (the last timed call's, -inf outside the windows) feed the top-k
+        line["topk"] = topk_block(fm, dev, stream, flush, out, inp, wl.name, min(args.steps, 20),
+                                  args.warmup, peaks["hbm_gbs"])
     if ws == 1 and not args.no_workloads:
         line["workloads"] = workload_block(fm, dev, stream, flush, min(args.steps, 20),
                                            args.warmup, fp8_peak, peaks["hbm_gbs"], sm_count)
@@ -475,6 +479,43 @@ def run_gpu(args):
     if ws > 1:
         torch.distributed.destroy_process_group()
     return 0
+
+
+def time_topk(fm, logits, k, steps, warmup, flush, stream, dev, win):
+    """Mean device time (ms) of `steps` fm.topk calls on `logits`, each after an L2 flush, CUDA
+    events on the launching stream; plus the clocks sampled meanwhile."""
+    import torch
+    for _ in range(warmup):
+        flush.zero_()
+        fm.topk(logits, k, stream=stream, **win)
+    torch.cuda.synchronize(dev)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    with ClockSampler(dev.index) as clocks:
+        host_lead(stream)
+        for i in range(steps):
+            flush.zero_()
+            starts[i].record(stream)
+            fm.topk(logits, k, stream=stream, **win)
+            ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+    return statistics.mean(s.elapsed_time(e) for s, e in zip(starts, ends)), clocks.summary()
+
+
+def topk_block(fm, dev, stream, flush, logits, inp, wl_name, steps, warmup, hbm_peak):
+    """The per-row top-k over the headline call's logits, at k = 512 and 2048, timed like
+    the headline: the indexer's consumer, so that its numbers are in the default line."""
+    M, N = inp["M"], inp["N"]
+    block = []
+    for k in TOPK_DEFAULT_KS:
+        ms, clocks = time_topk(fm, logits, k, steps, warmup, flush, stream, dev, {})
+        gbs = (M * N * 4 + M * k * 8) / (ms * 1e-3) / 1e9
+        kernel = topk_kernel_name(N, k)
+        block.append({"workload": wl_name, "k": k, "us_per_call": ms * 1e3, "gbs": gbs,
+                      "frac_of_hbm": gbs / hbm_peak, "kernel": kernel, "kernel_rev": TOPK_REV,
+                      "traffic": committed_traffic(kernel, wl_name, TOPK_REV, k),
+                      "steps": steps, "clocks": clocks})
+    return block
 
 
 def run_topk(args):
@@ -496,21 +537,8 @@ def run_topk(args):
     win = {"ks": t["ks"], "ke": t["ke"]} if args.windowed else {}
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
-    for _ in range(args.warmup):
-        flush.zero_()
-        fm.topk(logits, args.topk, stream=stream, **win)
-    torch.cuda.synchronize(dev)
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    with ClockSampler(dev.index) as clocks:
-        host_lead(stream)
-        for i in range(args.steps):
-            flush.zero_()
-            starts[i].record(stream)
-            fm.topk(logits, args.topk, stream=stream, **win)
-            ends[i].record(stream)
-        torch.cuda.synchronize(dev)
-    ms = statistics.mean(s.elapsed_time(e) for s, e in zip(starts, ends))
+    ms, clock_summary = time_topk(fm, logits, args.topk, args.steps, args.warmup, flush, stream,
+                                  dev, win)
     # bytes the call must move: the whole matrix, or only the windows when the top-k is windowed
     read_elems = workloads.valid_pairs(inp["ks"], inp["ke"], N) if args.windowed else M * N
     algo_bytes = read_elems * 4 + M * args.topk * 8
@@ -558,7 +586,7 @@ def run_topk(args):
                      else committed_traffic(kernel, wl.name, TOPK_REV, args.topk),
                      "peak_source": f"{peaks['source']} copy bandwidth",
                      "kernel": kernel, "kernel_rev": TOPK_REV},
-        "gpu_launches": args.steps, "clocks": clocks.summary(),
+        "gpu_launches": args.steps, "clocks": clock_summary,
     }), flush=True)
     return 0
 
@@ -651,6 +679,7 @@ def run_family_sweep(args):
 # Revision tags of the kernels the committed ncu traffic figures were taken on.
 KERNEL_REV = "v7"
 TOPK_REV = "t11"
+TOPK_DEFAULT_KS = (512, 2048)  # the top-k sizes the default line times
 
 
 def committed_traffic(kernel, workload, rev, k=None):
