@@ -200,6 +200,16 @@ def test_unaligned_rows_of_the_staged_row_path():
             _check(wide[:, off:off + n].copy(), k, gpu_rows=t, what=f"unaligned {off} k={k}")
 
 
+def test_unaligned_rows_of_the_long_row_kernels():
+    # rows that start off 16 bytes take the candidate pass's one-element-per-thread loop: rows
+    # of 20000 keys in the two-row kernels, of 70001 keys in the one-row kernel
+    wide = workloads.draw_logits(6, 70010, seed=23, neg_inf_frac=0.05)
+    for off, n in ((1, 20000), (3, 70001)):
+        t = torch.from_numpy(wide).cuda()[:, off:off + n]
+        for k in (64, 512, 2048):
+            _check(wide[:, off:off + n].copy(), k, gpu_rows=t, what=f"unaligned {off}+{n} k={k}")
+
+
 def _windows(M, N, rng):
     # random windows, with empty ones, windows off either end and whole rows
     a = rng.integers(-50, N + 50, size=M)
