@@ -67,11 +67,13 @@ template <bool kWin>
 bool topk_set_smem()
 {
     const auto attr = cudaFuncAttributeMaxDynamicSharedMemorySize;
-    return cudaFuncSetAttribute(topk_kernel<TopkSmemOne, kWin>, attr, int(sizeof(TopkSmemOne))) ==
-               cudaSuccess &&
-           cudaFuncSetAttribute(topk_kernel<TopkSmemPair, kWin>, attr,
+    return cudaFuncSetAttribute(topk_kernel<TopkSmemOne, kWin, 12>, attr,
+                                int(sizeof(TopkSmemOne))) == cudaSuccess &&
+           cudaFuncSetAttribute(topk_kernel<TopkSmemPair, kWin, 11>, attr,
                                 int(2 * sizeof(TopkSmemPair))) == cudaSuccess &&
-           cudaFuncSetAttribute(topk_kernel<TopkSmemPairWide, kWin>, attr,
+           cudaFuncSetAttribute(topk_kernel<TopkSmemPair, kWin, 12>, attr,
+                                int(2 * sizeof(TopkSmemPair))) == cudaSuccess &&
+           cudaFuncSetAttribute(topk_kernel<TopkSmemPairWide, kWin, 11>, attr,
                                 int(2 * sizeof(TopkSmemPairWide))) == cudaSuccess &&
            cudaFuncSetAttribute(topk_reg_kernel<kWin>, attr,
                                 int(kTopkRegRows * sizeof(TopkRegSmem))) == cudaSuccess;
@@ -93,15 +95,20 @@ void topk_launch(const TopkParams& p, int64_t M, int64_t N, int32_t k, int sm_co
         topk_reg_kernel<kWin><<<dim3(uint32_t(grid)), kTopkThreads,
                                 kTopkRegRows * sizeof(TopkRegSmem), s>>>(p);
     } else if (N <= 65536 && k <= 512) {
-        topk_kernel<TopkSmemPair, kWin><<<dim3(uint32_t(pair_grid)), kTopkThreads,
-                                          2 * sizeof(TopkSmemPair), s>>>(p);
+        // rows over 32768 keys sample into the finer histogram: a tighter threshold, fewer kept
+        if (N > 32768)
+            topk_kernel<TopkSmemPair, kWin, 12><<<dim3(uint32_t(pair_grid)), kTopkThreads,
+                                                  2 * sizeof(TopkSmemPair), s>>>(p);
+        else
+            topk_kernel<TopkSmemPair, kWin, 11><<<dim3(uint32_t(pair_grid)), kTopkThreads,
+                                                  2 * sizeof(TopkSmemPair), s>>>(p);
     } else if (N <= 32768) {
-        topk_kernel<TopkSmemPairWide, kWin><<<dim3(uint32_t(pair_grid)), kTopkThreads,
-                                              2 * sizeof(TopkSmemPairWide), s>>>(p);
+        topk_kernel<TopkSmemPairWide, kWin, 11><<<dim3(uint32_t(pair_grid)), kTopkThreads,
+                                                  2 * sizeof(TopkSmemPairWide), s>>>(p);
     } else {
         const int64_t grid = M < sm_count ? M : sm_count;
-        topk_kernel<TopkSmemOne, kWin><<<dim3(uint32_t(grid)), kTopkThreads,
-                                         sizeof(TopkSmemOne), s>>>(p);
+        topk_kernel<TopkSmemOne, kWin, 12><<<dim3(uint32_t(grid)), kTopkThreads,
+                                             sizeof(TopkSmemOne), s>>>(p);
     }
 }
 

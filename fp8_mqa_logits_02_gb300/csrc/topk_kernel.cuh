@@ -733,7 +733,8 @@ __device__ __forceinline__ void topk_keep_above(S& s, const float* x, int lo, in
     }
 }
 
-template <typename S, bool kWin>
+// kSBits: key bits of the sample's histogram (11: a quarter octave per bin; 12: an eighth).
+template <typename S, bool kWin, int kSBits>
 __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkParams p)
 {
     constexpr int NT = S::kNT;
@@ -759,7 +760,14 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkParams 
             s.n_cand = 0;
             s.n_tie = 0;
         }
-        for (int b = tid; b < kTopkBins; b += NT) s.hist[b] = 0u;
+        // the sample's histogram over the top kSBits key bits; beyond 11 bits it takes the
+        // per-warp histograms' space, free until the full select
+        static_assert(kSBits == 11 || kSBits == 12, "sample histogram bits");
+        static_assert(S::kHW * kTopkBins >= (1 << kSBits), "the sample histogram fits");
+        constexpr uint32_t n_sb = 1u << kSBits;
+        constexpr int s_shift = 32 - kSBits;
+        uint32_t* const shist = kSBits == 11 ? s.hist : &s.whist[0][0];
+        for (int b = tid; b < int(n_sb); b += NT) shist[b] = 0u;
         topk_sync<NT>();
         {
             const bool aligned = (reinterpret_cast<uintptr_t>(x) & 15u) == 0;
@@ -778,17 +786,17 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkParams 
                 }
 #pragma unroll
                 for (int c = 0; c < 8; ++c)
-                    if (topk_eligible(v[c])) atomicAdd(&s.hist[topk_key(v[c]) >> 21], 1u);
+                    if (topk_eligible(v[c])) atomicAdd(&shist[topk_key(v[c]) >> s_shift], 1u);
             }
         }
         topk_sync<NT>();
         // sampled keys needed above the threshold: an eighth of k plus about two standard
         // deviations of the sampled count
         const uint32_t r = (uint32_t(k) >> 3) + (uint32_t(k) >> 5) + 6u;
-        const bool lowest = topk_find_bin(s, s.hist, kTopkBins, r) < r;
+        const bool lowest = topk_find_bin(s, shist, n_sb, r) < r;
         float g = -3.402823466e38f;
         if (!lowest) {
-            const uint32_t kt = s.sel_bin << 21;  // a finite key: bins below 4 were not counted
+            const uint32_t kt = s.sel_bin << s_shift;  // a finite key: non-finite bins were not counted
             g = __uint_as_float((kt & 0x80000000u) ? (kt & 0x7FFFFFFFu) : ~kt);
         }
         topk_keep_above<S, kWin, 4>(s, x, lo, hi, g);
