@@ -678,7 +678,7 @@ def run_family_sweep(args):
 
 # Revision tags of the kernels the committed ncu traffic figures were taken on.
 KERNEL_REV = "v7"
-TOPK_REV = "t12"
+TOPK_REV = "t13"
 TOPK_DEFAULT_KS = (512, 2048)  # the top-k sizes the default line times
 
 

@@ -75,6 +75,8 @@ bool topk_set_smem()
                                 int(2 * sizeof(TopkSmemPair))) == cudaSuccess &&
            cudaFuncSetAttribute(topk_kernel<TopkSmemPairWide, kWin, 11>, attr,
                                 int(2 * sizeof(TopkSmemPairWide))) == cudaSuccess &&
+           cudaFuncSetAttribute(topk_kernel<TopkSmemPairWide, kWin, 12>, attr,
+                                int(2 * sizeof(TopkSmemPairWide))) == cudaSuccess &&
            cudaFuncSetAttribute(topk_reg_kernel<kWin>, attr,
                                 int(kTopkRegRows * sizeof(TopkRegSmem))) == cudaSuccess;
 }
@@ -103,8 +105,13 @@ void topk_launch(const TopkParams& p, int64_t M, int64_t N, int32_t k, int sm_co
             topk_kernel<TopkSmemPair, kWin, 11><<<dim3(uint32_t(pair_grid)), kTopkThreads,
                                                   2 * sizeof(TopkSmemPair), s>>>(p);
     } else if (N <= 32768) {
-        topk_kernel<TopkSmemPairWide, kWin, 11><<<dim3(uint32_t(pair_grid)), kTopkThreads,
-                                                  2 * sizeof(TopkSmemPairWide), s>>>(p);
+        // the finer sample histogram pays at k > 1024 once rows are longer than 8192 keys
+        if (k > 1024 && N > 8192)
+            topk_kernel<TopkSmemPairWide, kWin, 12><<<dim3(uint32_t(pair_grid)), kTopkThreads,
+                                                      2 * sizeof(TopkSmemPairWide), s>>>(p);
+        else
+            topk_kernel<TopkSmemPairWide, kWin, 11><<<dim3(uint32_t(pair_grid)), kTopkThreads,
+                                                      2 * sizeof(TopkSmemPairWide), s>>>(p);
     } else {
         const int64_t grid = M < sm_count ? M : sm_count;
         topk_kernel<TopkSmemOne, kWin, 12><<<dim3(uint32_t(grid)), kTopkThreads,
