@@ -125,10 +125,41 @@ def default_split(M: int, N: int, num_sms: int) -> int:
     return int(lib().fp8_mqa_logits_default_split(M, N, num_sms))
 
 
-def _stream_ptr(stream) -> int:
+# The current stream's raw handle in one call: torch.cuda.current_stream() builds a Stream
+# object each time, which costs several microseconds per launch on the small shapes.
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+_entries = {}
+
+
+def _stream_ptr(stream, device: torch.device | None = None) -> int:
+    """The cudaStream_t of ``stream``; when it is None, of the current stream of ``device``
+    (default: the current device)."""
     if stream is None:
-        stream = torch.cuda.current_stream()
+        idx = device.index if device is not None and device.index is not None \
+            else torch.cuda.current_device()
+        if _raw_stream is not None:
+            return int(_raw_stream(idx))
+        stream = torch.cuda.current_stream(idx)
     return int(stream.cuda_stream)
+
+
+def _entry(name: str):
+    """The library's entry point ``name``, resolved once per library build."""
+    key = (_debug, name)
+    fn = _entries.get(key)
+    if fn is None:
+        fn = getattr(lib(), name)
+        _entries[key] = fn
+    return fn
+
+
+def _on(dev: torch.device, fn, *args):
+    """``fn(*args)`` with ``dev`` the current CUDA device; the device is switched only when
+    it is not current already (the switch costs more than the check)."""
+    if torch.cuda.current_device() == dev.index:
+        return fn(*args)
+    with torch.cuda.device(dev):
+        return fn(*args)
 
 
 def _check(t: torch.Tensor, name: str, dtypes, ndim: int, device=None):
@@ -178,10 +209,9 @@ def fp8_mqa_logits(q: torch.Tensor, k: torch.Tensor, kv_scale: torch.Tensor, w: 
         _check(out, "out", (torch.float32,), 2, dev)
         if tuple(out.shape) != (M, N):
             raise ValueError(f"out must be [{M}, {N}]")
-    with torch.cuda.device(dev):
-        rc = lib().fp8_mqa_logits(q.data_ptr(), k.data_ptr(), kv_scale.data_ptr(), w.data_ptr(),
-                                  ks.data_ptr(), ke.data_ptr(), out.data_ptr(), M, N, H, D,
-                                  1 if clean_logits else 0, int(split_n), _stream_ptr(stream))
+    rc = _on(dev, _entry("fp8_mqa_logits"), q.data_ptr(), k.data_ptr(), kv_scale.data_ptr(),
+             w.data_ptr(), ks.data_ptr(), ke.data_ptr(), out.data_ptr(), M, N, H, D,
+             1 if clean_logits else 0, int(split_n), _stream_ptr(stream, dev))
     if rc != 0:
         raise Fp8MqaError(rc, "fp8_mqa_logits")
     return out
@@ -211,12 +241,11 @@ def topk(logits: torch.Tensor, k: int, with_values: bool = True, stream=None,
             raise ValueError(f"{name} must be a contiguous int32 [M] tensor on {dev}")
     idx = torch.empty((M, int(k)), dtype=torch.int32, device=dev)
     val = torch.empty((M, int(k)), dtype=torch.float32, device=dev) if with_values else None
-    with torch.cuda.device(dev):
-        rc = lib().fp8_mqa_topk_windowed(
-            logits.data_ptr(), M, N, logits.stride(0),
-            ks.data_ptr() if ks is not None else None, ke.data_ptr() if ke is not None else None,
-            int(k), idx.data_ptr(), val.data_ptr() if val is not None else None,
-            _stream_ptr(stream))
+    rc = _on(dev, _entry("fp8_mqa_topk_windowed"),
+             logits.data_ptr(), M, N, logits.stride(0),
+             ks.data_ptr() if ks is not None else None, ke.data_ptr() if ke is not None else None,
+             int(k), idx.data_ptr(), val.data_ptr() if val is not None else None,
+             _stream_ptr(stream, dev))
     if rc != 0:
         raise Fp8MqaError(rc, "fp8_mqa_topk_windowed")
     return idx, val
@@ -256,11 +285,10 @@ def fp8_mqa_logits_host(q, k, kv_scale, w, ks, ke, out, workspace: torch.Tensor,
     N = k.shape[0]
     if workspace.device.type != "cuda" or not workspace.is_contiguous():
         raise ValueError("workspace must be a contiguous CUDA tensor")
-    with torch.cuda.device(workspace.device):
-        rc = lib().fp8_mqa_logits_host(
-            q.data_ptr(), k.data_ptr(), kv_scale.data_ptr(), w.data_ptr(), ks.data_ptr(),
-            ke.data_ptr(), out.data_ptr(), M, N, H, D, 1 if clean_logits else 0, int(split_n),
-            workspace.data_ptr(), workspace.numel() * workspace.element_size(),
-            _stream_ptr(stream))
+    rc = _on(workspace.device, _entry("fp8_mqa_logits_host"),
+             q.data_ptr(), k.data_ptr(), kv_scale.data_ptr(), w.data_ptr(), ks.data_ptr(),
+             ke.data_ptr(), out.data_ptr(), M, N, H, D, 1 if clean_logits else 0, int(split_n),
+             workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+             _stream_ptr(stream, workspace.device))
     if rc != 0:
         raise Fp8MqaError(rc, "fp8_mqa_logits_host")
