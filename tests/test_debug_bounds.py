@@ -2,9 +2,9 @@
 
 Its kernel checks every global store and load, every TMA coordinate and every TMEM column
 before using it, and records the first violation in the status word instead of making the
-access (fp8_mqa_logits_check_error then returns FP8MQA_ERR_BOUNDS).  On this pool that build
-stands in for a memory checker ("Sanitizers").  The small cases of the
-parity suite run through it once: every call must record nothing and match the oracle.
+access (fp8_mqa_logits_check_error then returns FP8MQA_ERR_BOUNDS).  That build stands in
+for a memory checker, which cannot be run here.  The small cases of the parity suite run
+through it once: every call must record nothing and match the oracle.
 """
 import numpy as np
 import pytest

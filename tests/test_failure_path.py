@@ -6,8 +6,8 @@ separate bound), frees its tensor memory and exits, and the last CTA resets the 
 scheduler slot.  A short wait limit (fp8_mqa_logits_set_wait_limit_ns) makes the waits of a
 normal call run out.  The tests check that the call returns, that check_error reports
 FP8MQA_ERR_TIMEOUT, and that later calls on the same device -- through every scheduler slot,
-including the one the failed call used -- are correct again.  (SURVEY section 5's failure
-detection, in the allowed form: a bounded wait that gives up, no GPU fault.)
+including the one the failed call used -- are correct again.  (Failure detection in its
+safe form: a bounded wait that gives up, never a GPU fault.)
 """
 import numpy as np
 import pytest
