@@ -509,11 +509,14 @@ def topk_block(fm, dev, stream, flush, logits, inp, wl_name, steps, warmup, hbm_
     block = []
     for k in TOPK_DEFAULT_KS:
         ms, clocks = time_topk(fm, logits, k, steps, warmup, flush, stream, dev, {})
+        ms_unsorted, _ = time_topk(fm, logits, k, steps, warmup, flush, stream, dev,
+                                   {"sorted": False})
         gbs = (M * N * 4 + M * k * 8) / (ms * 1e-3) / 1e9
         kernel = topk_kernel_name(N, k)
         block.append({"workload": wl_name, "k": k, "us_per_call": ms * 1e3, "gbs": gbs,
                       "frac_of_hbm": gbs / hbm_peak, "kernel": kernel, "kernel_rev": TOPK_REV,
                       "traffic": committed_traffic(kernel, wl_name, TOPK_REV, k),
+                      "unsorted_us_per_call": ms_unsorted * 1e3,
                       "steps": steps, "clocks": clocks})
     return block
 
@@ -535,6 +538,8 @@ def run_topk(args):
     # --windowed: the logits without the -inf fill, and the top-k restricted to the windows
     logits = fm.fp8_mqa_logits(*largs, clean_logits=not args.windowed)
     win = {"ks": t["ks"], "ke": t["ke"]} if args.windowed else {}
+    if args.unsorted:
+        win["sorted"] = False
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
     ms, clock_summary = time_topk(fm, logits, args.topk, args.steps, args.warmup, flush, stream,
@@ -552,7 +557,7 @@ def run_topk(args):
         kw = {} if clean else {"ks": t["ks"], "ke": t["ke"]}
         def step():
             fm.fp8_mqa_logits(*largs, out=out, clean_logits=clean, stream=stream)
-            fm.topk(out, args.topk, stream=stream, **kw)
+            fm.topk(out, args.topk, stream=stream, sorted=not args.unsorted, **kw)
         for _ in range(args.warmup):
             flush.zero_()
             step()
@@ -575,7 +580,7 @@ def run_topk(args):
         "ms_per_step": ms, "us_per_call": ms * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": wl.name, "M": M, "N": N, "k": args.topk,
-                   "windowed": bool(args.windowed),
+                   "windowed": bool(args.windowed), "sorted": not args.unsorted,
                    "read_bytes": "windows only (clean_logits=0 logits)" if args.windowed
                    else "the whole matrix (clean_logits=1 logits)",
                    "l2": f"flushed before every timed call ({FLUSH_BYTES >> 20} MiB write)"},
@@ -724,6 +729,8 @@ def parse_args(argv=None):
                     help="time the per-row top-k (this k) over the workload's logits instead")
     ap.add_argument("--windowed", action="store_true",
                     help="with --topk: the windowed top-k over clean_logits=0 logits")
+    ap.add_argument("--unsorted", action="store_true",
+                    help="with --topk: each row's entries in selection order (no sort)")
     ap.add_argument("--family-sweep", action="store_true",
                     help="time every window family at the workload's shape instead")
     ap.add_argument("--sweep-split", default="",

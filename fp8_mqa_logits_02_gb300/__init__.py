@@ -56,6 +56,7 @@ SIGNATURES = {
                                               _I32, _I32, _I32, _P]),
     "fp8_mqa_topk": (ctypes.c_int, [_P, _I64, _I64, _I64, _I32, _P, _P, _P]),
     "fp8_mqa_topk_windowed": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _P, _I32, _P, _P, _P]),
+    "fp8_mqa_topk_ex": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _P, _I32, _I32, _P, _P, _P]),
 }
 
 TOPK_MAX_K = 2048
@@ -217,15 +218,20 @@ def fp8_mqa_logits(q: torch.Tensor, k: torch.Tensor, kv_scale: torch.Tensor, w: 
     return out
 
 
+TOPK_UNSORTED = 1  # fp8_mqa_topk_ex flag
+
+
 def topk(logits: torch.Tensor, k: int, with_values: bool = True, stream=None,
-         ks: torch.Tensor | None = None, ke: torch.Tensor | None = None):
+         ks: torch.Tensor | None = None, ke: torch.Tensor | None = None, sorted: bool = True):
     """Per-row top-k of a float32 [M, N] CUDA tensor (rows may be strided, elements not).
 
     Returns (indices int32 [M, k], values float32 [M, k] or None): the k largest finite
     entries of each row, by value descending and equal values by index ascending; slots past
     a row's finite entries hold -1 / -inf.  With ``ks``/``ke`` (int32 [M] on the same device,
     the windows the logits were made with) only entries in [ks[m], ke[m]) count and nothing
-    outside them is read, so the logits may come from ``clean_logits=False``.  Asynchronous on
+    outside them is read, so the logits may come from ``clean_logits=False``.  With
+    ``sorted=False`` each row holds the same entries in an unspecified order (the padding still
+    last), which skips the sort for consumers that take the indices as a set.  Asynchronous on
     ``stream``.
     """
     _check_strided_rows(logits, "logits")
@@ -241,13 +247,13 @@ def topk(logits: torch.Tensor, k: int, with_values: bool = True, stream=None,
             raise ValueError(f"{name} must be a contiguous int32 [M] tensor on {dev}")
     idx = torch.empty((M, int(k)), dtype=torch.int32, device=dev)
     val = torch.empty((M, int(k)), dtype=torch.float32, device=dev) if with_values else None
-    rc = _on(dev, _entry("fp8_mqa_topk_windowed"),
+    rc = _on(dev, _entry("fp8_mqa_topk_ex"),
              logits.data_ptr(), M, N, logits.stride(0),
              ks.data_ptr() if ks is not None else None, ke.data_ptr() if ke is not None else None,
-             int(k), idx.data_ptr(), val.data_ptr() if val is not None else None,
-             _stream_ptr(stream, dev))
+             int(k), 0 if sorted else TOPK_UNSORTED, idx.data_ptr(),
+             val.data_ptr() if val is not None else None, _stream_ptr(stream, dev))
     if rc != 0:
-        raise Fp8MqaError(rc, "fp8_mqa_topk_windowed")
+        raise Fp8MqaError(rc, "fp8_mqa_topk_ex")
     return idx, val
 
 

@@ -690,7 +690,15 @@ int fp8_mqa_topk_windowed(const float* logits, int64_t M, int64_t N, int64_t ld,
                           const int32_t* ks, const int32_t* ke, int32_t k, int32_t* indices,
                           float* values, void* stream)
 {
+    return fp8_mqa_topk_ex(logits, M, N, ld, ks, ke, k, 0, indices, values, stream);
+}
+
+int fp8_mqa_topk_ex(const float* logits, int64_t M, int64_t N, int64_t ld, const int32_t* ks,
+                    const int32_t* ke, int32_t k, int32_t flags, int32_t* indices, float* values,
+                    void* stream)
+{
     if (M < 0 || N < 0 || ld < N || k < 1 || k > fp8mqa::kTopkMaxK) return FP8MQA_ERR_INVALID_ARG;
+    if ((flags & ~int32_t(FP8MQA_TOPK_UNSORTED)) != 0) return FP8MQA_ERR_INVALID_ARG;
     if (N > (int64_t(1) << 30)) return FP8MQA_ERR_UNSUPPORTED_SHAPE;
     if (M == 0) return FP8MQA_OK;
     if (!indices || (N > 0 && !logits) || (ks == nullptr) != (ke == nullptr))
@@ -712,6 +720,7 @@ int fp8_mqa_topk_windowed(const float* logits, int64_t M, int64_t N, int64_t ld,
     p.values = values;
     p.ks = ks;
     p.ke = ke;
+    p.sorted = (flags & FP8MQA_TOPK_UNSORTED) ? 0 : 1;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (ks)
         fp8mqa::topk_launch<true>(p, M, N, k, st->sm_count, s);

@@ -50,6 +50,7 @@ struct TopkParams {
     float* values;     // [M, k] or null
     const int32_t* ks;  // row m's window [ks[m], ke[m]) clamped to [0, N); null: the whole row
     const int32_t* ke;
+    int32_t sorted;     // 1: each row's winners by value descending; 0: in selection order
 };
 
 // Row m's window, clamped to [0, N) (an empty window when ks >= ke).
@@ -950,7 +951,8 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_kernel(const TopkParams 
 
         // ---- 4. order the winners and write the row
         const int n_sel = int(min(s.n_cand, uint32_t(k)));
-        topk_sort_winners<NT>(s.cand, reinterpret_cast<unsigned long long*>(&s.whist[0][0]), n_sel);
+        if (p.sorted)
+            topk_sort_winners<NT>(s.cand, reinterpret_cast<unsigned long long*>(&s.whist[0][0]), n_sel);
         int32_t* oi = p.indices + row * int64_t(k);
         float* ov = p.values ? p.values + row * int64_t(k) : nullptr;
         for (int j = tid; j < k; j += NT) {
@@ -1206,7 +1208,7 @@ __global__ void __launch_bounds__(kTopkThreads, 1) topk_reg_kernel(const TopkPar
         const int n_sel = int(min(s.n_win, k));
 
         // ---- 4. order the winners and write the row
-        topk_sort_winners<NT>(s.win, s.cand, n_sel);
+        if (p.sorted) topk_sort_winners<NT>(s.win, s.cand, n_sel);
         int32_t* oi = p.indices + row * int64_t(k);
         float* ov = p.values ? p.values + row * int64_t(k) : nullptr;
         for (int j = tid; j < int(k); j += NT) {

@@ -245,6 +245,21 @@ FP8MQA_API int fp8_mqa_topk_windowed(const float* logits, int64_t M, int64_t N, 
                                      const int32_t* ks, const int32_t* ke, int32_t k,
                                      int32_t* indices, float* values, void* stream);
 
+/*
+ * fp8_mqa_topk_ex -- fp8_mqa_topk_windowed with flags.
+ *
+ *   flags    0, or FP8MQA_TOPK_UNSORTED: each row's result holds the same entries (the same
+ *            set of indices, each with its exact value), in an unspecified order that may differ
+ *            between calls; the padding still follows the selected entries.  This skips the
+ *            winners' sort, for consumers that take the indices as a set (sparse attention
+ *            gathers them).  Any other bit is FP8MQA_ERR_INVALID_ARG.
+ *   the other arguments and the errors are fp8_mqa_topk_windowed's.
+ */
+#define FP8MQA_TOPK_UNSORTED 1
+FP8MQA_API int fp8_mqa_topk_ex(const float* logits, int64_t M, int64_t N, int64_t ld,
+                               const int32_t* ks, const int32_t* ke, int32_t k, int32_t flags,
+                               int32_t* indices, float* values, void* stream);
+
 /* fp8_mqa_logits_strerror -- a static, human-readable name for a status code. */
 FP8MQA_API const char* fp8_mqa_logits_strerror(int status);
 

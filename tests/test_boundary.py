@@ -163,6 +163,15 @@ def test_topk_rejects_bad_arguments_before_device_work(lib):
     assert f(p, 4, 10, 10, 5, p, p + 1, None) == -3
 
 
+def test_topk_ex_rejects_unknown_flags_before_device_work(lib):
+    p = 0x1000
+    f = lib.fp8_mqa_topk_ex
+    assert f(p, 0, 10, 10, None, None, 5, 1, p, p, None) == 0       # no rows: nothing to do
+    assert f(p, 4, 10, 10, None, None, 5, 2, p, p, None) == -1      # an unknown flag bit
+    assert f(p, 4, 10, 10, None, None, 5, -1, p, p, None) == -1
+    assert f(p, 4, 10, 10, p, None, 5, 1, p, p, None) == -1         # ks without ke
+
+
 def test_windowed_topk_rejects_bad_arguments_before_device_work(lib):
     p = 0x1000
     f = lib.fp8_mqa_topk_windowed

@@ -210,6 +210,44 @@ def test_unaligned_rows_of_the_long_row_kernels():
             _check(wide[:, off:off + n].copy(), k, gpu_rows=t, what=f"unaligned {off}+{n} k={k}")
 
 
+def _check_unsorted(x, k, ks=None, ke=None, what=""):
+    # the unsorted result: per row the oracle's entries as a set, each index with its exact
+    # value, then the padding
+    M, N = x.shape
+    ref = x
+    if ks is not None:
+        ref = np.full_like(x, -np.inf)
+        for m in range(M):
+            lo, hi = max(int(ks[m]), 0), min(int(ke[m]), N)
+            if lo < hi:
+                ref[m, lo:hi] = x[m, lo:hi]
+    t = torch.from_numpy(x).cuda()
+    win = {} if ks is None else {"ks": torch.from_numpy(ks).cuda(), "ke": torch.from_numpy(ke).cuda()}
+    idx, val = fm.topk(t, k, sorted=False, **win)
+    torch.cuda.synchronize()
+    ri, _ = topk_rows(ref, k)
+    gi, gv = idx.cpu().numpy(), val.cpu().numpy()
+    for m in range(M):
+        n = int((ri[m] >= 0).sum())
+        assert set(gi[m, :n].tolist()) == set(ri[m, :n].tolist()), f"{what}: row {m} differs"
+        assert (gi[m, n:] == -1).all() and np.isneginf(gv[m, n:]).all(), f"{what}: row {m} padding"
+        assert np.array_equal(gv[m, :n].view(np.uint32), x[m, gi[m, :n]].view(np.uint32)), \
+            f"{what}: row {m} values"
+
+
+@pytest.mark.parametrize("M,N,k", [(300, 8192, 512), (100, 5000, 1024), (40, 300, 512),
+                                   (60, 20000, 512), (40, 20000, 2048), (40, 8192, 2048),
+                                   (6, 70000, 512), (6, 70000, 2048)])
+def test_unsorted_topk_selects_the_same_entries(M, N, k):
+    # every layout: the staged-row kernel, the two-row kernels (k <= 512 and wider), the
+    # one-row kernel; rows shorter than k get padding
+    x = workloads.draw_logits(M, N, seed=M + N + k, neg_inf_frac=0.2)
+    _check_unsorted(x, k, what=f"unsorted {M}x{N} k={k}")
+    rng = np.random.default_rng(N + k)
+    ks, ke = _windows(M, N, rng)
+    _check_unsorted(x, k, ks, ke, what=f"unsorted windowed {M}x{N} k={k}")
+
+
 def _windows(M, N, rng):
     # random windows, with empty ones, windows off either end and whole rows
     a = rng.integers(-50, N + 50, size=M)
