@@ -5,22 +5,26 @@
 //
 // For every row: the k largest finite logits (-inf, outside the row's window, is never
 // selected), ordered by value descending and, for equal values, by index ascending (-0.0
-// equals +0.0); slots past the row's finite entries get index -1 and value -inf.
+// equals +0.0); slots past the row's finite entries get index -1 and value -inf.  An unsorted
+// call (TopkParams::sorted = 0) writes the same entries in selection order, without the sort.
 //
 // Every kernel takes an optional window per row (fp8_mqa_topk_windowed): only entries inside
 // it are candidates, and nothing outside it is read.  Rows of up to 8192 keys at k <= 1024 go
 // to the staged-row kernel at the end of this file.  For the others, a persistent grid of at
-// most one CTA per SM walks the rows (a row's second read comes from L2): rows of up to 65536
-// keys at k <= 512, and of up to 32768 keys at larger k, two at a time, 256 threads each on a
-// named barrier of their own, so one row's barrier waits overlap the other's work; longer rows
-// one at a time with all 512 threads.  Each row
-// first tries a sampled threshold: a histogram of one 32-byte sector in eight of the window
-// gives G, one pass keeps the entries >= G in the buffer, and a radix cut over their
-// composites (key, index) picks the k winners.  That pass keeps the next chunk's loads in
-// flight while it examines the current one, and once it ends the next row's sample sectors
-// are prefetched into L2.  When that misses (fewer than k kept, or more
-// than the buffer holds), the row takes the full radix select on an order-preserving 32-bit
-// key:
+// most one CTA per SM walks the rows: rows of up to 65536 keys at k <= 512, and of up to
+// 32768 keys at larger k, two at a time, 256 threads each on a named barrier of their own, so
+// one row's barrier waits overlap the other's work; longer rows one at a time with all 512
+// threads.
+//
+// Each row first tries a sampled threshold.  A histogram of one 32-byte sector in eight of the
+// window (over the top 11 or 12 key bits, a template choice) gives G; one pass keeps the
+// entries >= G in a buffer, and a radix cut over their composites (key, index) picks the k
+// winners.  That pass keeps the next chunk's loads in flight while it examines the current
+// one, tests each float4 by its largest entry and lets a passing lane claim slots for its kept
+// entries with one shared-memory atomic; once it ends, the next row's sample sectors are
+// prefetched into L2.  When the threshold misses (fewer than k kept, or more than the buffer
+// holds), the row takes the full radix select on an order-preserving 32-bit key (its second
+// read of the row comes from L2):
 //   1. read the row, histogram the top 11 key bits (a private histogram per warp, so hot
 //      bins do not serialise the whole block);
 //   2. the bin b0 holding the k-th largest is found from the top;
