@@ -200,6 +200,18 @@ def test_unaligned_rows_of_the_staged_row_path():
             _check(wide[:, off:off + n].copy(), k, gpu_rows=t, what=f"unaligned {off} k={k}")
 
 
+@pytest.mark.parametrize("N", [8193, 32768, 32769, 65536, 65537])
+@pytest.mark.parametrize("k", [512, 2048])
+def test_row_lengths_at_the_dispatch_boundaries(N, k):
+    # each side of every switch between kernels and sample resolutions: at k <= 512 two rows
+    # per CTA up to 65536 keys (an 11-bit sample up to 32768, 12-bit beyond), then one row
+    # per CTA; at k > 512 two rows per CTA up to 32768 keys (a 12-bit sample beyond 8192 keys
+    # when k > 1024), then one row per CTA
+    x = workloads.draw_logits(4, N, seed=N % 1000 + k, neg_inf_frac=0.1)
+    _check(x, k, what=f"{N} keys k={k}")
+    _check_unsorted(x, k, what=f"unsorted {N} keys k={k}")
+
+
 def test_unaligned_rows_of_the_long_row_kernels():
     # rows that start off 16 bytes take the candidate pass's one-element-per-thread loop: rows
     # of 20000 keys in the two-row kernels, of 70001 keys in the one-row kernel
